@@ -1,0 +1,103 @@
+/*
+ * nf4.h - C ABI of the NF4 weight-only linear layer library (libnf4.so, NVIDIA GB300 / sm_103a).
+ *
+ * Format (deep-fold README, wertick01/deep-fold, format paragraph): weights are stored in groups of
+ * 64 consecutive in-features of one output row; each group holds 64 four-bit NF4 codes and one
+ * FP16 scale.  NF4 is the 16-value NormalFloat table introduced with QLoRA (deep-fold README,
+ * method paragraph; values published by Dettmers et al., 2023).  The library fixes what the pages
+ * leave open:
+ *   - codes[N][K/2] (uint8): weight (n, 2j) in the low nibble of byte (n, j), weight (n, 2j+1) in
+ *     the high nibble;
+ *   - scales[N][K/64] (IEEE binary16 bits): scale of group g of row n = fp16 round-to-nearest-even
+ *     of s = max |w[n][64g .. 64g+63]| computed in fp32;
+ *   - code of w = the index i minimising the fp32 distance |fp32(w / s) - T[i]|, ties to the lower
+ *     index; an all-zero group (s = 0) gets code 7 (T[7] = 0);
+ *   - dequantized weight w_hat = bf16_rn(fp32(T[code] * float(scale)));
+ *   - y[m][n] = bf16_rn(sum_k x[m][k] * w_hat[n][k]) with at least fp32 accumulation.  Accepted
+ *     results satisfy |y - y64| <= 2^-8 |y64| + 2^-12 sum_k |x[m][k] w_hat[n][k]|, y64 being the
+ *     same sum in exact products and double-precision addition.
+ *
+ * Common rules for every entry point:
+ *   - Pointers are device pointers owned by the caller, row-major and contiguous, each aligned to
+ *     16 bytes.  bf16 and fp16 values travel as their 16-bit patterns (uint16_t).
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).  No call synchronises
+ *     the device, allocates memory or keeps state beyond a per-device capability check.
+ *   - Arguments are checked on the host before anything is launched; on an error nothing is
+ *     launched and no output is written.  A failed launch returns NF4_ERR_CUDA and leaves the CUDA
+ *     error state cleared.
+ *   - Shapes: N and M may be 0 (nothing is launched, NF4_OK); K must be a positive multiple of 64;
+ *     M, N and K must each be at most 2^31 - 1.
+ *   - Non-finite inputs are outside the contract: results are unspecified, but no call faults.
+ *   - The same inputs give the same output bytes on every call (no atomics, fixed reduction order).
+ */
+#ifndef NF4_H
+#define NF4_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NF4_GROUP_SIZE 64
+#define NF4_ABI_VERSION 1
+
+typedef enum nf4_status {
+    NF4_OK = 0,
+    NF4_ERR_NULL = 1,               /* a required pointer is NULL */
+    NF4_ERR_SHAPE = 2,              /* negative size, K not a positive multiple of 64, or > 2^31-1 */
+    NF4_ERR_ALIGN = 3,              /* a pointer is not 16-byte aligned */
+    NF4_ERR_ALIAS = 4,              /* an output range overlaps an input range */
+    NF4_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 (sm_103) */
+    NF4_ERR_CUDA = 6                /* a CUDA runtime call or kernel launch failed */
+} nf4_status;
+
+/*
+ * nf4_quantize - pack fp32 weights into NF4 codes and fp16 group scales.
+ * Defines: the format paragraph of the deep-fold README (64-weight groups, 4-bit NF4 codes, one
+ * FP16 scale); the pages do this offline in their compressor, here it is a device kernel.
+ *   w       in   float [N][K]
+ *   codes   out  uint8 [N][K/2]   low nibble first
+ *   scales  out  fp16 bits [N][K/64]
+ * codes and scales must not overlap w or each other.
+ */
+nf4_status nf4_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
+                        cudaStream_t stream);
+
+/*
+ * nf4_dequant - expand packed weights to a dense bf16 matrix (a test and inspection entry point:
+ * the linear layer below never writes this matrix, as the execution-path table of the deep-fold
+ * README requires).
+ *   codes   in   uint8 [N][K/2]
+ *   scales  in   fp16 bits [N][K/64]
+ *   w_hat   out  bf16 bits [N][K], w_hat = bf16_rn(fp32(T[code] * float(scale)))
+ */
+nf4_status nf4_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                       uint16_t* w_hat, cudaStream_t stream);
+
+/*
+ * nf4_linear - y = x * w_hat^T with the weights streamed in packed form and dequantized tile by
+ * tile on chip (deep-fold README, execution-path table: N=1 decode GEMV, prefill GEMM of up to 32
+ * positions; larger M is this library's extension).  M = 1 runs a CUDA-core GEMV, small M a
+ * CUDA-core kernel, large M a tcgen05 tensor-core GEMM; the choice depends on M only.
+ *   x       in   bf16 bits [M][K]
+ *   codes   in   uint8 [N][K/2]
+ *   scales  in   fp16 bits [N][K/64]
+ *   y       out  bf16 bits [M][N]; must not overlap x, codes or scales
+ */
+nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* nf4_status_str(nf4_status status);
+
+/* NF4_ABI_VERSION of the built library. */
+int nf4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4_H */
