@@ -1,0 +1,128 @@
+"""NF4 weight-only linear layer for NVIDIA GB300 (sm_103a): thin Python binding of libnf4.so.
+
+The library (``csrc/``, C ABI in ``include/nf4.h``) does all the work.  This module only marshals
+torch tensors (device memory and streams) into the C calls of the same names and raises
+``NF4Error`` on a non-OK status.  There is no CPU fallback: if ``libnf4.so`` has not been built
+(``nf4_weight_only_gb300.build.build()``), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GROUP = 64
+LIB_PATH = _build.LIB_PATH
+
+STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_ALIGN",
+                4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA"}
+
+# Every symbol include/nf4.h declares.
+EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_status_str", "nf4_abi_version")
+
+
+class NF4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libnf4.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with nf4_weight_only_gb300.build.build() "
+                           "(no CPU fallback exists)")
+    lib = ctypes.CDLL(p)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.nf4_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.nf4_quantize.restype = ci
+    lib.nf4_dequant.argtypes = [vp, vp, i64, i64, vp, vp]
+    lib.nf4_dequant.restype = ci
+    lib.nf4_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.nf4_linear.restype = ci
+    lib.nf4_status_str.argtypes = [ci]
+    lib.nf4_status_str.restype = ctypes.c_char_p
+    lib.nf4_abi_version.argtypes = []
+    lib.nf4_abi_version.restype = ci
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    try:
+        return load().nf4_status_str(status).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(status, f"status {status}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise NF4Error(status, what)
+
+
+def nf4_quantize(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """w fp32 [N, K] -> codes uint8 [N, K/2], scales fp16 [N, K/64] (all CUDA tensors)."""
+    n, k = w.shape
+    _check(load().nf4_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(stream)), "nf4_quantize")
+
+
+def nf4_dequant(codes: torch.Tensor, scales: torch.Tensor, w_hat: torch.Tensor, stream=None) -> None:
+    """codes [N, K/2], scales [N, K/64] -> w_hat bf16 [N, K]."""
+    n, k = codes.shape[0], codes.shape[1] * 2
+    _check(load().nf4_dequant(_ptr(codes), _ptr(scales), n, k, _ptr(w_hat), _stream(stream)), "nf4_dequant")
+
+
+def nf4_linear(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
+               stream=None) -> None:
+    """y[M, N] = x[M, K] * w_hat^T (bf16 in, bf16 out)."""
+    m, k = x.shape
+    n = codes.shape[0]
+    _check(load().nf4_linear(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
+           "nf4_linear")
+
+
+# Convenience wrappers that allocate the outputs with torch.
+def quantize(w: torch.Tensor, stream=None):
+    n, k = w.shape
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((n, k // GROUP), dtype=torch.float16, device=w.device)
+    nf4_quantize(w, codes, scales, stream)
+    return codes, scales
+
+
+def dequant(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:
+    w_hat = torch.empty((codes.shape[0], codes.shape[1] * 2), dtype=torch.bfloat16, device=codes.device)
+    nf4_dequant(codes, scales, w_hat, stream)
+    return w_hat
+
+
+def linear(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:
+    y = torch.empty((x.shape[0], codes.shape[0]), dtype=torch.bfloat16, device=x.device)
+    nf4_linear(x, codes, scales, y, stream)
+    return y

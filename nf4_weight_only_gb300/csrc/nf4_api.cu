@@ -1,0 +1,138 @@
+// C ABI of libnf4.so: argument checks, the per-device capability check and the M-based dispatch.
+#include <atomic>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+#include "../../include/nf4.h"
+#include "nf4_internal.h"
+
+namespace nf4 {
+int64_t gemv_max_k(int64_t M);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+// Per-device cache: 0 = unknown, -1 = unsupported, otherwise the SM count of a 10.3 device.
+std::atomic<int> g_device_sms[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a_bytes > 0 && b_bytes > 0 && a0 < b0 + static_cast<uintptr_t>(b_bytes) &&
+           b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+nf4_status check_k(int64_t K) {
+    if (K <= 0 || K % NF4_GROUP_SIZE != 0 || K > kMaxDim) return NF4_ERR_SHAPE;
+    return NF4_OK;
+}
+
+// Current device must be compute capability 10.3; returns its SM count through `sms`.
+nf4_status current_device(int* device, int* sms) {
+    if (cudaGetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return NF4_ERR_CUDA;
+    }
+    if (*device < 0 || *device >= kMaxDevices) return NF4_ERR_UNSUPPORTED_DEVICE;
+    int cached = g_device_sms[*device].load(std::memory_order_relaxed);
+    if (cached == 0) {
+        int major = 0, minor = 0, count = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess) {
+            cudaGetLastError();
+            return NF4_ERR_CUDA;
+        }
+        cached = (major == 10 && minor == 3 && count > 0) ? count : -1;
+        g_device_sms[*device].store(cached, std::memory_order_relaxed);
+    }
+    if (cached < 0) return NF4_ERR_UNSUPPORTED_DEVICE;
+    *sms = cached;
+    return NF4_OK;
+}
+
+nf4_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return NF4_OK;
+    cudaGetLastError();
+    return NF4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nf4_status_str(nf4_status status) {
+    switch (status) {
+        case NF4_OK: return "NF4_OK";
+        case NF4_ERR_NULL: return "NF4_ERR_NULL: a required pointer is NULL";
+        case NF4_ERR_SHAPE: return "NF4_ERR_SHAPE: bad size (K must be a positive multiple of 64; sizes <= 2^31-1)";
+        case NF4_ERR_ALIGN: return "NF4_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case NF4_ERR_ALIAS: return "NF4_ERR_ALIAS: an output overlaps an input";
+        case NF4_ERR_UNSUPPORTED_DEVICE: return "NF4_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+        case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA call or launch failed";
+    }
+    return "NF4 status: unknown code";
+}
+
+int nf4_abi_version(void) { return NF4_ABI_VERSION; }
+
+nf4_status nf4_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
+                        cudaStream_t stream) {
+    if (N < 0 || N > kMaxDim) return NF4_ERR_SHAPE;
+    nf4_status st = check_k(K);
+    if (st != NF4_OK) return st;
+    if (N == 0) return NF4_OK;
+    if (!w || !codes || !scales) return NF4_ERR_NULL;
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales)) return NF4_ERR_ALIGN;
+    const int64_t wb = N * K * 4, cb = N * K / 2, sb = N * (K / NF4_GROUP_SIZE) * 2;
+    if (overlap(codes, cb, w, wb) || overlap(scales, sb, w, wb) || overlap(codes, cb, scales, sb))
+        return NF4_ERR_ALIAS;
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
+    return from_cuda(nf4::launch_quantize(w, N, K, codes, scales, sms, stream));
+}
+
+nf4_status nf4_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int64_t K, uint16_t* w_hat,
+                       cudaStream_t stream) {
+    if (N < 0 || N > kMaxDim) return NF4_ERR_SHAPE;
+    nf4_status st = check_k(K);
+    if (st != NF4_OK) return st;
+    if (N == 0) return NF4_OK;
+    if (!codes || !scales || !w_hat) return NF4_ERR_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(w_hat)) return NF4_ERR_ALIGN;
+    const int64_t ob = N * K * 2, cb = N * K / 2, sb = N * (K / NF4_GROUP_SIZE) * 2;
+    if (overlap(w_hat, ob, codes, cb) || overlap(w_hat, ob, scales, sb)) return NF4_ERR_ALIAS;
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
+    return from_cuda(nf4::launch_dequant(codes, scales, N, K, w_hat, sms, stream));
+}
+
+nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y, int64_t M,
+                      int64_t N, int64_t K, cudaStream_t stream) {
+    if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim) return NF4_ERR_SHAPE;
+    nf4_status st = check_k(K);
+    if (st != NF4_OK) return st;
+    if (M == 0 || N == 0) return NF4_OK;
+    if (!x || !codes || !scales || !y) return NF4_ERR_NULL;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y)) return NF4_ERR_ALIGN;
+    const int64_t yb = M * N * 2, xb = M * K * 2, cb = N * K / 2, sb = N * (K / NF4_GROUP_SIZE) * 2;
+    if (overlap(y, yb, x, xb) || overlap(y, yb, codes, cb) || overlap(y, yb, scales, sb)) return NF4_ERR_ALIAS;
+    if (K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;  // widest K the kernels cover
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
+    if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
+    // Token chunks of at most four through the CUDA-core family.
+    for (int64_t t0 = 0; t0 < M; t0 += nf4::kGemvMaxTokens) {
+        const int64_t mt = (M - t0) < nf4::kGemvMaxTokens ? (M - t0) : nf4::kGemvMaxTokens;
+        st = from_cuda(nf4::launch_gemv(x + t0 * K, codes, scales, y + t0 * N, mt, N, K, sms, stream));
+        if (st != NF4_OK) return st;
+    }
+    return NF4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,23 @@
+// Launchers shared between the C-ABI layer and the kernel translation units (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace nf4 {
+
+// Each launcher enqueues its kernels on `stream` and returns the result of cudaGetLastError()
+// (cudaSuccess when nothing was launched).  Arguments are validated by the caller.
+cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
+                            int num_sms, cudaStream_t stream);
+cudaError_t launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                           uint16_t* w_hat, int num_sms, cudaStream_t stream);
+// CUDA-core GEMV family: y[M, N] for 1 <= M <= kGemvMaxTokens.
+constexpr int kGemvMaxTokens = 4;
+cudaError_t launch_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
+                        int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t stream);
+
+// Per-device constant table used by the GEMV (built once per device, stream-ordered).
+cudaError_t ensure_tables(int device, cudaStream_t stream);
+
+}  // namespace nf4

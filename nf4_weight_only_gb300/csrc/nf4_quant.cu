@@ -1,0 +1,132 @@
+// NF4 quantize (pack) and dequantize kernels for sm_103a.
+//
+// Both are HBM-bound streaming kernels.  Because K is a multiple of 64, group g of row n is the
+// flat group n * (K/64) + g: its 64 weights, 32 code bytes and one scale are contiguous, so both
+// kernels walk a flat group index with a grid-stride loop.
+#include "nf4_device.cuh"
+#include "nf4_internal.h"
+
+namespace nf4 {
+namespace {
+
+// Ordered integer key of a binary32 value (increases with the value; -0 and +0 share key 0).
+__device__ __forceinline__ int32_t f32_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? -static_cast<int32_t>(b & 0x7FFFFFFFu) : static_cast<int32_t>(b);
+}
+
+__device__ __forceinline__ float key_f32(int32_t k) {
+    return __uint_as_float(k >= 0 ? static_cast<uint32_t>(k) : (0x80000000u | static_cast<uint32_t>(-k)));
+}
+
+// Decision threshold between codes i and i+1: the smallest binary32 r in [T[i], T[i+1]] that is
+// strictly closer, in fp32 distance, to T[i+1] than to T[i].  Between the two table values the fp32
+// distance to T[i] never decreases and the distance to T[i+1] never increases as r grows, so the
+// predicate flips exactly once and bisection over the ordered bit patterns finds the flip.  The
+// nearest-code rule "argmin_i |r - T[i]| in fp32, ties to the lower index" is then exactly
+// code(r) = number of thresholds <= r.
+__device__ float decision_threshold(int i) {
+    const float t_lo = kNF4[i], t_hi = kNF4[i + 1];
+    int32_t lo = f32_key(t_lo), hi = f32_key(t_hi);
+    while (hi - lo > 1) {
+        const int32_t mid = lo + (hi - lo) / 2;
+        const float r = key_f32(mid);
+        const bool upper = fabsf(__fsub_rn(r, t_hi)) < fabsf(__fsub_rn(r, t_lo));
+        if (upper)
+            hi = mid;
+        else
+            lo = mid;
+    }
+    return key_f32(hi);
+}
+
+// Four-step binary search over the 15 sorted thresholds.
+__device__ __forceinline__ uint32_t code_of(float r, const float* thr) {
+    uint32_t c = (r >= thr[7]) ? 8u : 0u;
+    c += (r >= thr[c + 3]) ? 4u : 0u;
+    c += (r >= thr[c + 1]) ? 2u : 0u;
+    c += (r >= thr[c]) ? 1u : 0u;
+    return c;
+}
+
+// One warp per group: lane l holds weights 2l and 2l+1 and writes code byte l.
+__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ w, int64_t groups,
+                                                       uint8_t* __restrict__ codes,
+                                                       uint16_t* __restrict__ scales) {
+    __shared__ float thr[16];
+    if (threadIdx.x < 15) thr[threadIdx.x] = decision_threshold(threadIdx.x);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < groups;
+         g += warps) {
+        const float2 v = __ldcs(reinterpret_cast<const float2*>(w + g * kGroup) + lane);
+        float s = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+        uint32_t byte = 0x77u;  // an all-zero group: code 7 (T[7] = 0) everywhere
+        if (s != 0.0f) {
+            const uint32_t c0 = code_of(__fdiv_rn(v.x, s), thr);
+            const uint32_t c1 = code_of(__fdiv_rn(v.y, s), thr);
+            byte = c0 | (c1 << 4);
+        }
+        codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte);
+        if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s));
+    }
+}
+
+// Each thread expands 8 code bytes (16 weights, a quarter group) into 32 bytes of bf16.
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ codes,
+                                                      const uint16_t* __restrict__ scales, int64_t groups,
+                                                      uint16_t* __restrict__ w_hat) {
+    __shared__ float table[16];
+    if (threadIdx.x < 16) table[threadIdx.x] = kNF4[threadIdx.x];
+    __syncthreads();
+    const int64_t quarters = groups * 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < quarters; q += stride) {
+        const uint2 cw = __ldcs(reinterpret_cast<const uint2*>(codes) + q);
+        const float s = __half2float(__ushort_as_half(scales[q >> 2]));
+        uint32_t out[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t byte = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
+            const uint32_t lo = bf16_bits(__fmul_rn(table[byte & 0xFu], s));
+            const uint32_t hi = bf16_bits(__fmul_rn(table[byte >> 4], s));
+            out[j] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(w_hat + q * 16);
+        __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
+        __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    }
+}
+
+int grid_for(int64_t items_per_block_units, int64_t units, int num_sms, int blocks_per_sm) {
+    int64_t blocks = (units + items_per_block_units - 1) / items_per_block_units;
+    int64_t cap = static_cast<int64_t>(num_sms) * blocks_per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
+                            int num_sms, cudaStream_t stream) {
+    const int64_t groups = N * (K / kGroup);
+    if (groups == 0) return cudaSuccess;
+    const int grid = grid_for(8, groups, num_sms, 8);  // 8 warps (groups) per 256-thread block
+    quantize_kernel<<<grid, 256, 0, stream>>>(w, groups, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
+                           uint16_t* w_hat, int num_sms, cudaStream_t stream) {
+    const int64_t groups = N * (K / kGroup);
+    if (groups == 0) return cudaSuccess;
+    const int grid = grid_for(256, groups * 4, num_sms, 8);
+    dequant_kernel<<<grid, 256, 0, stream>>>(codes, scales, groups, w_hat);
+    return cudaGetLastError();
+}
+
+}  // namespace nf4

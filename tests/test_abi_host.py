@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads, exports every symbol
+that include/nf4.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nf4_weight_only_gb300 import build
+    path = build.build()
+    import nf4_weight_only_gb300 as nf4
+    return nf4.load(path)
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "nf4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert {"nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_status_str", "nf4_abi_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/nf4.h but not exported"
+    import nf4_weight_only_gb300 as nf4
+    assert set(nf4.EXPORTED) == set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.nf4_abi_version() == 1
+    for code in range(7):
+        s = lib.nf4_status_str(code).decode()
+        assert s.startswith("NF4_")
+    assert b"unknown" in lib.nf4_status_str(99)
+
+
+# Fake, never-dereferenced device addresses: every case below fails validation first.
+A = 0x7F0000000000
+B = 0x7F1000000000
+C = 0x7F2000000000
+D = 0x7F3000000000
+vp = ctypes.c_void_p
+
+
+def linear(lib, x, codes, scales, y, m, n, k):
+    return lib.nf4_linear(vp(x), vp(codes), vp(scales), vp(y), m, n, k, None)
+
+
+@pytest.mark.parametrize("m,n,k,want", [
+    (1, 1, 0, 2), (1, 1, 63, 2), (1, 1, 96, 2), (-1, 4, 64, 2), (1, -4, 64, 2),
+    (1, 1, -64, 2), (1 << 31, 1, 64, 2), (1, 1 << 31, 64, 2), (1, 1, 1 << 40, 2),
+])
+def test_linear_shape_errors(lib, m, n, k, want):
+    assert linear(lib, A, B, C, D, m, n, k) == want
+
+
+def test_linear_empty_is_ok_without_device(lib):
+    assert linear(lib, 0, 0, 0, 0, 0, 5, 64) == 0
+    assert linear(lib, 0, 0, 0, 0, 3, 0, 64) == 0
+
+
+def test_linear_null_align_alias(lib):
+    assert linear(lib, 0, B, C, D, 1, 4, 64) == 1
+    assert linear(lib, A, B, 0, D, 1, 4, 64) == 1
+    assert linear(lib, A + 2, B, C, D, 1, 4, 64) == 3
+    assert linear(lib, A, B + 8, C, D, 1, 4, 64) == 3
+    assert linear(lib, A, B, C, D + 4, 1, 4, 64) == 3
+    # y overlapping x, codes or scales
+    assert linear(lib, A, B, C, A + 64, 1, 4, 64) == 4
+    assert linear(lib, A, B, C, B + 16, 1, 4, 64) == 4
+    assert linear(lib, A, B, C, C, 1, 4, 64) == 4
+
+
+def test_quantize_dequant_errors(lib):
+    q = lib.nf4_quantize
+    assert q(vp(A), 4, 100, vp(B), vp(C), None) == 2
+    assert q(vp(A), -1, 64, vp(B), vp(C), None) == 2
+    assert q(vp(0), 4, 64, vp(B), vp(C), None) == 1
+    assert q(vp(A + 4), 4, 64, vp(B), vp(C), None) == 3
+    assert q(vp(A), 4, 64, vp(A + 512), vp(C), None) == 4   # codes inside w
+    assert q(vp(A), 4, 64, vp(B), vp(B + 16), None) == 4    # scales inside codes
+    assert q(vp(0), 0, 64, vp(0), vp(0), None) == 0        # empty
+    d = lib.nf4_dequant
+    assert d(vp(B), vp(C), 4, 65, vp(D), None) == 2
+    assert d(vp(B), vp(0), 4, 64, vp(D), None) == 1
+    assert d(vp(B), vp(C), 4, 64, vp(D + 2), None) == 3
+    assert d(vp(B), vp(C), 4, 64, vp(B), None) == 4
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    """Past validation the library asks the runtime for the device; with no GPU it must return an
+    error status (never crash)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert linear(lib, A, B, C, D, 1, 4, 64) in (5, 6)
+
+
+def test_binding_raises_without_library(tmp_path):
+    import nf4_weight_only_gb300 as nf4
+    with pytest.raises(RuntimeError, match="missing"):
+        nf4.load(str(tmp_path / "nope.so"))

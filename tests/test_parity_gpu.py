@@ -1,0 +1,237 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+quantize and dequant must be bit-exact; the linear must meet the per-element bound
+|y - y64| <= 2^-8 |y64| + 2^-12 sum_k |x_k w_k|.
+"""
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as P
+from gpu_util import DEV, Guarded, bf16_to_dev, dev_to_bits, f16_dev_to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nf4():
+    import nf4_weight_only_gb300 as m
+    from nf4_weight_only_gb300 import build
+    build.build()
+    m.load()
+    return m
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.default()
+
+
+def gpu_quantize(nf4, w: np.ndarray):
+    codes, scales = nf4.quantize(torch.from_numpy(w).to(DEV))
+    return codes, scales
+
+
+# ------------------------------------------------------------------------------------------------
+# quantize
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("n,k,seed,outliers", [
+    (2048, 2048, 0, 0.0),      # the single 2048x2048 linear
+    (1, 64, 1, 0.0), (7, 128, 2, 0.0), (257, 320, 3, 0.0), (33, 2112, 4, 0.0),
+    (300, 6144, 5, 0.01),      # 20B-prefill-style outliers
+])
+def test_quantize_bit_exact(nf4, o, n, k, seed, outliers):
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(seed, n, k, outlier_frac=outliers)
+    w[0, :64] = 0.0                # an all-zero group
+    if n > 1:
+        w[1, 64:128] *= 1e-6       # tiny scale (fp16 subnormal range)
+    codes, scales = gpu_quantize(nf4, w)
+    c_ref, s_ref = o.quantize(w)
+    assert np.array_equal(f16_dev_to_bits(scales), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+
+
+def _oracle_codes(args):
+    lo, hi = args
+    keys = np.arange(lo, hi, dtype=np.int64)
+    bits = np.where(keys >= 0, keys, 0x80000000 | (-keys)).astype(np.uint32)
+    return lo, oracle.default().nf4_code(bits.view(np.float32))
+
+
+def test_quantize_every_r_in_unit_interval(nf4):
+    """Every binary32 r in [-1, 1]: groups whose first weight is 1.0 have s = 1 exactly, so the
+    other 63 weights are their own normalised values r and the kernel's code must equal the
+    oracle's nearest code of r."""
+    lo, hi = P.ordered_key(np.float32(-1.0)), P.ordered_key(np.float32(1.0)) + 1
+    per_group = 63
+    chunk = per_group * (1 << 18)  # 16.5M values per chunk
+    starts = list(range(lo, hi, chunk))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(16, os.cpu_count() or 1)) as pool:
+        jobs = pool.imap(_oracle_codes, [(a, min(a + chunk, hi)) for a in starts])
+        for a in starts:
+            b = min(a + chunk, hi)
+            keys = np.arange(a, b, dtype=np.int64)
+            bits = np.where(keys >= 0, keys, 0x80000000 | (-keys)).astype(np.uint32)
+            groups = (bits.size + per_group - 1) // per_group
+            w = np.zeros((groups, 64), np.float32)
+            w[:, 0] = 1.0
+            flat = w[:, 1:].reshape(-1)
+            flat[:bits.size] = bits.view(np.float32)
+            w[:, 1:] = flat.reshape(groups, per_group)
+            codes, scales = gpu_quantize(nf4, w)
+            got = P.unpack_low_nibble_first(codes.cpu().numpy())[:, 1:].reshape(-1)[:bits.size]
+            a2, want = next(jobs)
+            assert a2 == a
+            bad = np.flatnonzero(got != want)
+            assert bad.size == 0, f"code differs at r={bits.view(np.float32)[bad[0]]!r}: gpu {got[bad[0]]} oracle {want[bad[0]]}"
+            assert np.all(f16_dev_to_bits(scales) == 0x3C00)
+
+
+def test_quantize_large_sampled_rows(nf4, o):
+    """A 5120 x 27648 matrix (the 32B-shaped down projection) generated on the device: sampled rows
+    copied back as fp32 are re-quantized by the oracle."""
+    from nf4_weight_only_gb300 import synth
+    w = synth.device_weights(123, 5120, 27648, DEV)
+    codes, scales = nf4.quantize(w)
+    rows = np.array([0, 1, 2047, 4095, 5119])
+    w_rows = w[rows].cpu().numpy()
+    c_ref, s_ref = o.quantize(w_rows)
+    assert np.array_equal(codes[rows].cpu().numpy(), c_ref)
+    assert np.array_equal(f16_dev_to_bits(scales[rows]), s_ref)
+
+
+# ------------------------------------------------------------------------------------------------
+# dequant
+# ------------------------------------------------------------------------------------------------
+def test_dequant_every_code_and_scale(nf4, o):
+    """All 16 codes against all 65536 fp16 scale patterns (non-finite ones included: both sides
+    compute the same IEEE product; NaN payloads are compared as NaN only)."""
+    scale_bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    row = np.array([c | ((15 - c) << 4) for c in range(16)] * 2, np.uint8)
+    codes = np.tile(row, (scale_bits.size, 1))
+    w_hat = nf4.dequant(torch.from_numpy(codes).to(DEV),
+                        torch.from_numpy(scale_bits.view(np.int16)).view(torch.float16).to(DEV)[:, None].contiguous())
+    got = dev_to_bits(w_hat)
+    want = o.dequant(codes, scale_bits[:, None])
+    gnan = (got & 0x7F80 == 0x7F80) & (got & 0x7F != 0)
+    wnan = (want & 0x7F80 == 0x7F80) & (want & 0x7F != 0)
+    assert np.array_equal(gnan, wnan)
+    assert np.array_equal(got[~gnan], want[~wnan])
+
+
+@pytest.mark.parametrize("n,k,seed", [(2048, 2048, 0), (1, 64, 1), (257, 320, 2), (64, 11008, 3)])
+def test_dequant_bit_exact(nf4, o, n, k, seed):
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(seed, n, k, outlier_frac=0.01)
+    c_ref, s_ref = o.quantize(w)
+    out = Guarded((n, k), torch.bfloat16)
+    nf4.nf4_dequant(torch.from_numpy(c_ref).to(DEV),
+                    torch.from_numpy(s_ref.view(np.int16)).view(torch.float16).to(DEV), out.t)
+    assert np.array_equal(dev_to_bits(out.t), o.dequant(c_ref, s_ref))
+    assert out.canaries_intact()
+
+
+# ------------------------------------------------------------------------------------------------
+# linear
+# ------------------------------------------------------------------------------------------------
+def run_linear(nf4, x_bits, codes, scales):
+    m, n = x_bits.shape[0], codes.shape[0]
+    out = Guarded((m, n), torch.bfloat16)
+    nf4.nf4_linear(bf16_to_dev(x_bits), torch.from_numpy(codes).to(DEV),
+                   torch.from_numpy(scales.view(np.int16)).view(torch.float16).to(DEV), out.t)
+    torch.cuda.synchronize()
+    assert out.canaries_intact(), "nf4_linear wrote outside y"
+    return dev_to_bits(out.t)
+
+
+def check_linear(nf4, o, m, n, k, seed, outliers=0.0, nthreads=16):
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(seed, n, k, outlier_frac=outliers)
+    x = synth.activations_bf16(seed + 1000, m, k)
+    codes, scales = o.quantize(w)
+    y = run_linear(nf4, x, codes, scales)
+    y64, mag = o.linear(x, codes, scales, nthreads=nthreads)
+    ok, ratio, mask = oracle.within_tolerance(y, y64, mag)
+    assert ok, f"M={m} N={n} K={k}: {np.count_nonzero(~mask)} outside tolerance, worst ratio {ratio:.3f}"
+    return ratio
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("n,k", [(1, 64), (7, 128), (257, 2048), (96, 5120), (40, 11008), (24, 13824)])
+def test_linear_small_shapes(nf4, o, m, n, k):
+    check_linear(nf4, o, m, n, k, seed=n * 31 + k)
+
+
+def test_linear_single_2048(nf4, o):
+    """The single 2048 x 2048 linear, M = 1, seed 0."""
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(0, 2048, 2048)
+    x = synth.activations_bf16(1000, 1, 2048)
+    codes, scales = o.quantize(w)
+    y = run_linear(nf4, x, codes, scales)
+    y64, mag = o.linear(x, codes, scales, nthreads=16)
+    ok, ratio, _ = oracle.within_tolerance(y, y64, mag)
+    assert ok, ratio
+
+
+def test_linear_k27648_m1(nf4, o):
+    check_linear(nf4, o, 1, 160, 27648, seed=5)
+
+
+def test_linear_m33_outliers(nf4, o):
+    check_linear(nf4, o, 33, 130, 6144, seed=6, outliers=0.01)
+
+
+def test_linear_zero_input_and_zero_rows(nf4, o):
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(9, 64, 512)
+    w[3] = 0.0
+    codes, scales = o.quantize(w)
+    x = np.zeros((2, 512), np.uint16)
+    y = run_linear(nf4, x, codes, scales)
+    assert np.all((y & 0x7FFF) == 0)
+    x = synth.activations_bf16(10, 1, 512)
+    y = run_linear(nf4, x, codes, scales)
+    assert (y[0, 3] & 0x7FFF) == 0
+
+
+def test_linear_deterministic(nf4, o):
+    from nf4_weight_only_gb300 import synth
+    w = synth.weights(11, 300, 5120)
+    x = synth.activations_bf16(12, 3, 5120)
+    codes, scales = o.quantize(w)
+    y1 = run_linear(nf4, x, codes, scales)
+    y2 = run_linear(nf4, x, codes, scales)
+    assert np.array_equal(y1, y2)
+
+
+def test_empty_is_noop(nf4):
+    y = torch.full((4,), 7.0, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros((1, 32), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((1, 1), dtype=torch.float16, device=DEV)
+    lib = nf4.load()
+    import ctypes
+    st = lib.nf4_linear(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(codes.data_ptr()),
+                        ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(y.data_ptr()), 0, 1, 64, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+def test_bad_alignment_rejected_on_device_pointers(nf4):
+    import ctypes
+    lib = nf4.load()
+    x = torch.zeros((1, 128 + 8), dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros((4, 64), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((4, 2), dtype=torch.float16, device=DEV)
+    y = torch.zeros((1, 4), dtype=torch.bfloat16, device=DEV)
+    st = lib.nf4_linear(ctypes.c_void_p(x.data_ptr() + 2), ctypes.c_void_p(codes.data_ptr()),
+                        ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(y.data_ptr()), 1, 4, 128, None)
+    assert st == 3  # NF4_ERR_ALIGN
