@@ -83,6 +83,53 @@ __device__ __forceinline__ uint16_t ld_nc_u16(const uint16_t* p) {
     return v;
 }
 
+// Integer work steered onto the FMA pipe (IMAD) instead of the half-rate ALU pipe.  ptxas turns a
+// multiply by a compile-time constant into a shift or logic op, so the multipliers arrive as
+// kernel arguments whose values it cannot see: m1 = 0xFFFFFFFF, p16 = 0x10000.
+__device__ __forceinline__ uint32_t not_fma(uint32_t w, uint32_t m1) {  // w * -1 + -1 = ~w
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %2;" : "=r"(d) : "r"(w), "r"(m1));
+    return d;
+}
+__device__ __forceinline__ uint32_t shr16_fma(uint32_t w, uint32_t p16) {  // hi32(w * 2^16) = w >> 16
+    uint32_t d;
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(p16));
+    return d;
+}
+__device__ __forceinline__ uint32_t shl4_fma(uint32_t w) {  // w << 4 (ptxas keeps constant left shifts on IMAD)
+    uint32_t d;
+    asm("mul.lo.u32 %0, %1, 16;" : "=r"(d) : "r"(w));
+    return d;
+}
+
+// 16-byte asynchronous global -> shared copy; bytes past `src_bytes` (0..16) are zero-filled.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint32_t src_bytes = 16) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Programmatic dependent launch: let the next grid in the stream start launching, and wait until
+// the previous grid has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 v;
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }

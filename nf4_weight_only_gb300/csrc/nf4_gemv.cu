@@ -32,9 +32,12 @@ namespace {
 
 constexpr int kRows = 4;       // rows per warp iteration
 constexpr int kMaxWarps = 16;  // warps per CTA (slices x row lanes)
+constexpr int kStages = 2;     // per-warp shared-memory ring depth (row quads in flight)
+constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
-// V table: row m holds {L(0..3), L(4..7), L(8..11), L(12..15)} and {H(0..3), ..., H(12..15)},
-// L / H being the low / high byte of the bf16 entry V[m][c].
+// V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
+// the same order, L / H being the low / high byte of the bf16 entry V[m][c].  Codes 8..15 are stored
+// in reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.
 __device__ uint4 g_vtab[1024 * 2];
 
 __global__ void build_vtab_kernel() {
@@ -45,26 +48,29 @@ __global__ void build_vtab_kernel() {
 #pragma unroll
     for (int c = 0; c < 16; c++) {
         const uint32_t b = bf16_bits(__fmul_rn(kNF4[c], s1));
-        lo[c >> 2] |= (b & 0xFFu) << (8 * (c & 3));
-        hi[c >> 2] |= (b >> 8) << (8 * (c & 3));
+        const int slot = c < 8 ? c : 8 + (15 - c);  // byte position inside the 16-byte plane
+        lo[slot >> 2] |= (b & 0xFFu) << (8 * (slot & 3));
+        hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
     }
     g_vtab[2 * m] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     g_vtab[2 * m + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
 // Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order.
-__device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4& th, uint32_t out[4]) {
-    const uint32_t wb = w ^ 0x88888888u;  // bit 3 flipped: codes 8-15 index the second half
-    const uint32_t w4 = w << 4;
+// 18 ALU-pipe instructions (PRMT / LOP3) and 4 FMA-pipe ones (selector preparation).
+__device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4& th, uint32_t m1, uint32_t p16,
+                                        uint32_t out[4]) {
+    const uint32_t nw = not_fma(w, m1);  // nibble 15 - c: codes 8..15 index the reversed second half
+    const uint32_t w4 = shl4_fma(w);
+    const uint32_t wh = shr16_fma(w, p16), nwh = shr16_fma(nw, p16);
     uint32_t msk = prmt(w4, w, 0xD9C8u);  // byte i = 0xFF iff code i >= 8 (i = 0..3)
-    uint32_t lo = select_bits(prmt(tl.x, tl.y, w), prmt(tl.z, tl.w, wb), msk);
-    uint32_t hi = select_bits(prmt(th.x, th.y, w), prmt(th.z, th.w, wb), msk);
+    uint32_t lo = select_bits(prmt(tl.x, tl.y, w), prmt(tl.z, tl.w, nw), msk);
+    uint32_t hi = select_bits(prmt(th.x, th.y, w), prmt(th.z, th.w, nw), msk);
     out[0] = prmt(lo, hi, 0x5140u);
     out[1] = prmt(lo, hi, 0x7362u);
-    const uint32_t wh = w >> 16, wbh = wb >> 16;
     msk = prmt(w4, w, 0xFBEAu);  // codes 4..7
-    lo = select_bits(prmt(tl.x, tl.y, wh), prmt(tl.z, tl.w, wbh), msk);
-    hi = select_bits(prmt(th.x, th.y, wh), prmt(th.z, th.w, wbh), msk);
+    lo = select_bits(prmt(tl.x, tl.y, wh), prmt(tl.z, tl.w, nwh), msk);
+    hi = select_bits(prmt(th.x, th.y, wh), prmt(th.z, th.w, nwh), msk);
     out[2] = prmt(lo, hi, 0x5140u);
     out[3] = prmt(lo, hi, 0x7362u);
 }
@@ -96,30 +102,72 @@ __device__ __forceinline__ float reduce_transposed(float (&v)[V], int lane) {
 
 __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
 
-// MT tokens; LPG lanes per 64-weight group (1 or 2).
+template <int MT, int LPG>
+struct GemvShape {
+    static constexpr int WPL = kGroup / LPG;   // weights per lane per row
+    static constexpr int CB = WPL / 2;         // code bytes per lane per row
+    static constexpr int CHUNKS = CB / 16;     // 16-byte copies per lane per row
+    static constexpr int GPW = 32 / LPG;       // groups per warp slice
+    static constexpr int SWIN = 2 * GPW + 16;  // bytes of a row's 16-byte-aligned scale window
+    static constexpr int STAGE_CODES = kRows * 32 * CB;
+    static constexpr int STAGE = STAGE_CODES + kRows * SWIN;
+    static constexpr int WARP_SMEM = kStages * STAGE;
+};
+
+// MT tokens; LPG lanes per 64-weight group (1 or 2).  Shared memory: the V table (32 KB), then one
+// private ring of kStages row quads per warp (codes and scale windows, filled with cp.async), then
+// two [S][Q*kRows][MT] slice-partial buffers when S > 1.
 template <int MT, int LPG>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
-                const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int N, int K, int S, int Q) {
-    constexpr int WPL = kGroup / LPG;  // weights per lane
-    constexpr int WORDS = WPL / 8;     // code words per lane per row
-    constexpr int GPW = 32 / LPG;      // groups per warp slice
+                const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int N, int K, int S, int Q,
+                uint32_t m1, uint32_t p16) {
+    using SH = GemvShape<MT, LPG>;
     constexpr int V = pow2_ceil(kRows * MT);
-    extern __shared__ float red[];  // [S][Q * kRows][MT] slice partials
+    extern __shared__ __align__(16) uint8_t smem[];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
     const int s = warp % S, q = warp / S;
     const int G = K / kGroup;
-    const int g = s * GPW + lane / LPG;
+    const int g = s * SH::GPW + lane / LPG;
     const bool active = g < G;
-    const int k0 = s * GPW * kGroup + lane * WPL;
+    const int k0 = s * SH::GPW * kGroup + lane * SH::WPL;
+    const int g_hi = min(G, (s + 1) * SH::GPW);        // one past the slice's last group
+    const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;  // 16-byte chunk swizzle: conflict-free reads
+    const uint4* vtab = reinterpret_cast<const uint4*>(smem);
+    uint8_t* ring = smem + kVtabBytes + warp * SH::WARP_SMEM;
+    float* red = reinterpret_cast<float*>(smem + kVtabBytes + nwarps * SH::WARP_SMEM);
+    const int rows_per_block = Q * kRows;
+    const int64_t nblocks = (static_cast<int64_t>(N) + rows_per_block - 1) / rows_per_block;
+    const int64_t my_blocks =
+        blockIdx.x < nblocks ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t row_bytes = static_cast<uint32_t>(K / 2);
+    const uint32_t row_sbytes = static_cast<uint32_t>(G * 2);
+    const int64_t scale_bytes = static_cast<int64_t>(N) * row_sbytes;
+    const uint8_t* scale_base = reinterpret_cast<const uint8_t*>(scales);
+    const int64_t rstep = static_cast<int64_t>(gridDim.x) * rows_per_block;
 
-    uint32_t xr[MT][WPL / 2];
+    // Let the next kernel in the stream launch, warm L2 with this warp's first rows (a prefetch
+    // never returns stale data: L2 is coherent), copy the constant table, then wait for the
+    // previous kernel's results.
+    pdl_launch_dependents();
+    const int64_t r_first = static_cast<int64_t>(blockIdx.x) * rows_per_block + q * kRows;
+    if (my_blocks > 0 && active) {
+#pragma unroll
+        for (int j = 0; j < kRows; j++)
+            if (r_first + j < N) prefetch_l2(codes + (r_first + j) * row_bytes + k0 / 2);
+    }
+    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(smem)[i] = ld_ca_v4(&g_vtab[i]);
+    pdl_wait();
+
+    uint32_t xr[MT][SH::WPL / 2];
 #pragma unroll
     for (int t = 0; t < MT; t++) {
 #pragma unroll
-        for (int i = 0; i < WPL / 8; i++) {
+        for (int i = 0; i < SH::WPL / 8; i++) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (active) v = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K + k0 + 8 * i);
             xr[t][4 * i + 0] = v.x;
@@ -128,74 +176,113 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             xr[t][4 * i + 3] = v.w;
         }
     }
+    __syncthreads();  // V table ready
 
-    const int rows_per_block = Q * kRows;
-    const int64_t row_stride = K / 2;
-    for (int64_t rb = blockIdx.x; rb * rows_per_block < N; rb += gridDim.x) {
-        const int64_t r0 = rb * rows_per_block + static_cast<int64_t>(q) * kRows;
-        uint32_t cw[kRows][WORDS];
-        uint16_t sc[kRows];
+    // Enqueue the copies of this warp's t-th row quad into ring stage t % kStages (one commit group
+    // per quad, empty past the end so that group counting stays uniform).
+    auto issue = [&](int64_t t) {
+        if (t < my_blocks) {
+            uint8_t* st = ring + static_cast<int>(t % kStages) * SH::STAGE;
+            const int64_t r0 = r_first + t * rstep;
+            const uint8_t* src = codes + r0 * row_bytes + k0 / 2;
+            int64_t sfirst = (r0 * G + s * SH::GPW) * 2;  // first scale byte of the row's slice
 #pragma unroll
-        for (int j = 0; j < kRows; j++) {
-            const int64_t r = r0 + j;
-            const bool ok = active && r < N;
-            const uint8_t* p = codes + r * row_stride + k0 / 2;
+            for (int j = 0; j < kRows; j++) {
+                if (r0 + j < N) {
+                    if (active) {
 #pragma unroll
-            for (int i = 0; i < WORDS / 4; i++) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (ok) v = ld_nc_v4(p + 16 * i);
-                cw[j][4 * i + 0] = v.x;
-                cw[j][4 * i + 1] = v.y;
-                cw[j][4 * i + 2] = v.z;
-                cw[j][4 * i + 3] = v.w;
+                        for (int c = 0; c < SH::CHUNKS; c++)
+                            cp_async16(st + ((j * 32 + lane) * SH::CHUNKS + (c ^ sw)) * 16, src + 16 * c);
+                    }
+                    const int64_t a = sfirst & ~static_cast<int64_t>(15);
+                    const int64_t chunk = a + 16 * lane;
+                    if (chunk < sfirst + 2 * (g_hi - s * SH::GPW)) {
+                        const int64_t left = scale_bytes - chunk;
+                        cp_async16(st + SH::STAGE_CODES + j * SH::SWIN + 16 * lane, scale_base + chunk,
+                                   static_cast<uint32_t>(left < 16 ? left : 16));
+                    }
+                }
+                src += row_bytes;
+                sfirst += row_sbytes;
             }
-            sc[j] = ok ? ld_nc_u16(scales + r * G + g) : static_cast<uint16_t>(0);
         }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int t = 0; t < kStages - 1; t++) issue(t);
+
+    for (int64_t t = 0; t < my_blocks; t++) {
+        issue(t + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint8_t* st = ring + static_cast<int>(t % kStages) * SH::STAGE;
+        const int64_t r0 = r_first + t * rstep;
+        // Row j's scale window starts at its first scale byte rounded down to 16; the lane's scale
+        // sits (first byte mod 16) + 2 * (g - first group) bytes into it.
+        const int f0lo = static_cast<int>(((r0 * G + s * SH::GPW) * 2) & 15);
+        const int goff = 2 * (g - s * SH::GPW);
+        const int rlo = static_cast<int>(row_sbytes & 15u);
         float part[V];
 #pragma unroll
         for (int i = 0; i < V; i++) part[i] = 0.0f;
 #pragma unroll
         for (int j = 0; j < kRows; j++) {
-            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc[j])));
+            if (r0 + j >= N) continue;  // warp-uniform
+            uint32_t sc = 0;
+            if (active) {
+                const int off = ((f0lo + j * rlo) & 15) + goff;
+                sc = *reinterpret_cast<const uint16_t*>(st + SH::STAGE_CODES + j * SH::SWIN + off);
+            }
+            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
             const uint32_t m = (sb >> 13) & 0x3FFu;
             const float pow2 = __uint_as_float(sb & 0x7F800000u);  // 2^E, or 0 for a zero scale
-            const uint4 tl = ld_ca_v4(&g_vtab[2 * m]);
-            const uint4 th = ld_ca_v4(&g_vtab[2 * m + 1]);
+            const uint4 tl = vtab[2 * m];
+            const uint4 th = vtab[2 * m + 1];
             float a0[MT], a1[MT];
 #pragma unroll
-            for (int t = 0; t < MT; t++) a0[t] = a1[t] = 0.0f;
+            for (int tt = 0; tt < MT; tt++) a0[tt] = a1[tt] = 0.0f;
 #pragma unroll
-            for (int wi = 0; wi < WORDS; wi++) {
-                uint32_t wp[4];
-                lookup8(cw[j][wi], tl, th, wp);
+            for (int c = 0; c < SH::CHUNKS; c++) {
+                const uint4 cw = lds128(st + ((j * 32 + lane) * SH::CHUNKS + (c ^ sw)) * 16);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-                for (int t = 0; t < MT; t++) {
+                for (int wi = 0; wi < 4; wi++) {
+                    uint32_t wp[4];
+                    lookup8(words[wi], tl, th, m1, p16, wp);
 #pragma unroll
-                    for (int p = 0; p < 4; p++) fma_bf16x2(a0[t], a1[t], wp[p], xr[t][4 * wi + p]);
+                    for (int tt = 0; tt < MT; tt++) {
+#pragma unroll
+                        for (int p = 0; p < 4; p++)
+                            fma_bf16x2(a0[tt], a1[tt], wp[p], xr[tt][4 * (4 * c + wi) + p]);
+                    }
                 }
             }
 #pragma unroll
-            for (int t = 0; t < MT; t++) part[j * MT + t] = (a0[t] + a1[t]) * pow2;
+            for (int tt = 0; tt < MT; tt++) part[j * MT + tt] = (a0[tt] + a1[tt]) * pow2;
         }
+        __syncwarp();  // every lane is done with this stage before it is refilled
         const float total = reduce_transposed<V>(part, lane);
         constexpr int lanes_per_value = 32 / V;
         const int idx = lane / lanes_per_value;
         const bool writer = (lane % lanes_per_value) == 0 && idx < kRows * MT;
-        const int j = idx / MT, t = idx % MT;
+        const int j = idx / MT, tt = idx % MT;
         if (S == 1) {
-            if (writer && r0 + j < N) y[static_cast<int64_t>(t) * N + r0 + j] = bf16_bits(total);
+            if (writer && r0 + j < N) y[static_cast<int64_t>(tt) * N + r0 + j] = bf16_bits(total);
         } else {
-            if (writer) red[(s * rows_per_block + q * kRows + j) * MT + t] = total;
+            const int64_t rb = blockIdx.x + t * gridDim.x;
+            float* buf = red + (t & 1) * S * rows_per_block * MT;
+            if (writer) buf[(s * rows_per_block + q * kRows + j) * MT + tt] = total;
             __syncthreads();
             for (int i = threadIdx.x; i < rows_per_block * MT; i += blockDim.x) {
                 const int64_t r = rb * rows_per_block + i / MT;
                 float acc = 0.0f;
-                for (int ss = 0; ss < S; ss++) acc += red[ss * rows_per_block * MT + i];
+                for (int ss = 0; ss < S; ss++) acc += buf[ss * rows_per_block * MT + i];
                 if (r < N) y[static_cast<int64_t>(i % MT) * N + r] = bf16_bits(acc);
             }
-            __syncthreads();
         }
     }
+    cp_async_wait<0>();
 }
 
 struct TableState {
@@ -207,18 +294,42 @@ TableState g_tables;
 template <int MT, int LPG>
 cudaError_t launch_gemv_t(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
                           int64_t N, int64_t K, int num_sms, cudaStream_t stream) {
+    using SH = GemvShape<MT, LPG>;
     const int G = static_cast<int>(K / kGroup);
-    const int gpw = 32 / LPG;
-    const int S = (G + gpw - 1) / gpw;
-    const int Q = S >= kMaxWarps ? 1 : kMaxWarps / S;
-    const int threads = 32 * S * Q;
+    const int S = (G + SH::GPW - 1) / SH::GPW;
+    // Row lanes per slice: enough CTAs to cover the SMs when N is small, at most kMaxWarps warps.
+    const int64_t quads = (N + kRows - 1) / kRows;
+    int Q = static_cast<int>((quads + num_sms - 1) / num_sms);
+    const int qmax = S >= kMaxWarps ? 1 : kMaxWarps / S;
+    if (Q > qmax) Q = qmax;
+    if (Q < 1) Q = 1;
+    const int warps = S * Q;
     const int rows_per_block = Q * kRows;
     const int64_t blocks_needed = (N + rows_per_block - 1) / rows_per_block;
-    const int64_t grid = blocks_needed < num_sms ? blocks_needed : num_sms;
-    const size_t smem = S > 1 ? static_cast<size_t>(S) * rows_per_block * MT * sizeof(float) : 0;
-    gemv_kernel<MT, LPG><<<static_cast<int>(grid), threads, smem, stream>>>(
-        x, codes, scales, y, static_cast<int>(N), static_cast<int>(K), S, Q);
-    return cudaGetLastError();
+    const int grid = static_cast<int>(blocks_needed < num_sms ? blocks_needed : num_sms);
+    const size_t smem = kVtabBytes + static_cast<size_t>(warps) * SH::WARP_SMEM +
+                        (S > 1 ? 2 * static_cast<size_t>(S) * rows_per_block * MT * sizeof(float) : 0);
+    static bool attr_set = false;  // the largest request is set once per process
+    if (!attr_set) {
+        const size_t max_smem = kVtabBytes + static_cast<size_t>(kMaxWarps) * SH::WARP_SMEM +
+                                2 * static_cast<size_t>(kMaxWarps) * kRows * MT * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT, LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(max_smem));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * warps);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, codes, scales, y, static_cast<int>(N),
+                              static_cast<int>(K), S, Q, 0xFFFFFFFFu, 0x10000u);
 }
 
 }  // namespace
