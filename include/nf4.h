@@ -90,6 +90,15 @@ nf4_status nf4_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, 
 nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/*
+ * nf4_check_device_error - diagnostics: read and clear the device-side error word of the current
+ * device.  The tensor-core path bounds every pipeline wait (about one second); a wait that runs
+ * out records a nonzero code there, and the kernel drains and exits instead of hanging.  *code
+ * receives that code (0 = none).  This call waits for the device (it is not meant for the hot
+ * path).
+ */
+nf4_status nf4_check_device_error(int* code);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* nf4_status_str(nf4_status status);
 

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_
                 4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA"}
 
 # Every symbol include/nf4.h declares.
-EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_status_str", "nf4_abi_version")
+EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_check_device_error", "nf4_status_str",
+            "nf4_abi_version")
 
 
 class NF4Error(RuntimeError):
@@ -53,6 +54,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_linear.restype = ci
     lib.nf4_status_str.argtypes = [ci]
     lib.nf4_status_str.restype = ctypes.c_char_p
+    lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.nf4_check_device_error.restype = ci
     lib.nf4_abi_version.argtypes = []
     lib.nf4_abi_version.restype = ci
     if path is None:
@@ -105,6 +108,13 @@ def nf4_linear(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: to
     n = codes.shape[0]
     _check(load().nf4_linear(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
            "nf4_linear")
+
+
+def nf4_check_device_error() -> int:
+    """Read and clear the device error word (0 = no pipeline wait timed out).  Synchronizes."""
+    code = ctypes.c_int(0)
+    _check(load().nf4_check_device_error(ctypes.byref(code)), "nf4_check_device_error")
+    return code.value
 
 
 # Convenience wrappers that allocate the outputs with torch.

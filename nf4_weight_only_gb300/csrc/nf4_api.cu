@@ -81,6 +81,15 @@ const char* nf4_status_str(nf4_status status) {
 
 int nf4_abi_version(void) { return NF4_ABI_VERSION; }
 
+nf4_status nf4_check_device_error(int* code) {
+    if (!code) return NF4_ERR_NULL;
+    *code = 0;
+    int dev = 0, sms = 0;
+    nf4_status st = current_device(&dev, &sms);
+    if (st != NF4_OK) return st;
+    return from_cuda(nf4::read_and_clear_error(code));
+}
+
 nf4_status nf4_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,
                         cudaStream_t stream) {
     if (N < 0 || N > kMaxDim) return NF4_ERR_SHAPE;
@@ -122,17 +131,12 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y)) return NF4_ERR_ALIGN;
     const int64_t yb = M * N * 2, xb = M * K * 2, cb = N * K / 2, sb = N * (K / NF4_GROUP_SIZE) * 2;
     if (overlap(y, yb, x, xb) || overlap(y, yb, codes, cb) || overlap(y, yb, scales, sb)) return NF4_ERR_ALIAS;
-    if (K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;  // widest K the kernels cover
+    if (M < nf4::kTcMinTokens && K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
     if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
-    // Token chunks of at most four through the CUDA-core family.
-    for (int64_t t0 = 0; t0 < M; t0 += nf4::kGemvMaxTokens) {
-        const int64_t mt = (M - t0) < nf4::kGemvMaxTokens ? (M - t0) : nf4::kGemvMaxTokens;
-        st = from_cuda(nf4::launch_gemv(x + t0 * K, codes, scales, y + t0 * N, mt, N, K, sms, stream));
-        if (st != NF4_OK) return st;
-    }
-    return NF4_OK;
+    if (M >= nf4::kTcMinTokens) return from_cuda(nf4::launch_tc(x, codes, scales, y, M, N, K, stream));
+    return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
 }
 
 }  // extern "C"

@@ -24,6 +24,8 @@
 // fixed order, so results are deterministic.  The grid is persistent over row blocks.
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "nf4_device.cuh"
 #include "nf4_internal.h"
 
@@ -37,13 +39,20 @@ constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
 // V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
 // the same order, L / H being the low / high byte of the bf16 entry V[m][c].  Codes 8..15 are stored
-// in reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.
-__device__ uint4 g_vtab[1024 * 2];
+// in reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.  Rows are laid
+// out in blocks of eight: the eight low-byte chunks, then the eight high-byte chunks, so the chunk
+// of row m sits at index m + (m & ~7) (+ 8 for the high bytes) and eight lanes reading random rows
+// spread over all eight 16-byte bank groups of a 128-byte line.
+// Rows 1024..2047 repeat the table at twice the value (V[m][c] * 2, exact), which the tensor-core
+// path uses to fold an odd scale exponent into the table.
+__device__ uint4 g_vtab[2048 * 2];
 
 __global__ void build_vtab_kernel() {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;
-    if (m >= 1024) return;
-    const float s1 = __uint_as_float(0x3F800000u | (static_cast<uint32_t>(m) << 13));  // 1 + m/1024
+    const int m = blockIdx.x * blockDim.x + threadIdx.x;  // table row: 1024 * p + mantissa class
+    if (m >= 2048) return;
+    // (1 + (m mod 1024)/1024) * 2^(m / 1024), exactly
+    const float s1 = __uint_as_float((0x3F800000u + (static_cast<uint32_t>(m >> 10) << 23)) |
+                                     (static_cast<uint32_t>(m & 1023) << 13));
     uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int c = 0; c < 16; c++) {
@@ -52,8 +61,8 @@ __global__ void build_vtab_kernel() {
         lo[slot >> 2] |= (b & 0xFFu) << (8 * (slot & 3));
         hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
     }
-    g_vtab[2 * m] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    g_vtab[2 * m + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    g_vtab[m + (m & ~7)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    g_vtab[m + (m & ~7) + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
 // Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order.
@@ -236,9 +245,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             }
             const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
             const uint32_t m = (sb >> 13) & 0x3FFu;
-            const float pow2 = __uint_as_float(sb & 0x7F800000u);  // 2^E, or 0 for a zero scale
-            const uint4 tl = vtab[2 * m];
-            const uint4 th = vtab[2 * m + 1];
+            const float pow2 = __uint_as_float(sb & 0xFF800000u);  // +-2^E, or 0 for a zero scale
+            const uint4 tl = vtab[m + (m & ~7u)];
+            const uint4 th = vtab[m + (m & ~7u) + 8];
             float a0[MT], a1[MT];
 #pragma unroll
             for (int tt = 0; tt < MT; tt++) a0[tt] = a1[tt] = 0.0f;
@@ -333,6 +342,101 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint8_t* codes, const uint16_
 }
 
 }  // namespace
+}  // namespace nf4
+
+#include "nf4_tc.cuh"
+
+namespace nf4 {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+template <int T>
+cudaError_t launch_tc_t(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y, int64_t M,
+                        int64_t N, int64_t K, cudaStream_t stream) {
+    using L = tc::Layout<T>;
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap tx, tcodes;
+    {   // x: bf16 [M][K], boxes of 64 (K) x T (tokens), 128-byte swizzle; rows past M read as zero
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(T)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {   // codes: u8 [N][K/2], boxes of 32 bytes (one group) x 128 rows; rows past N read as zero
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(tc::kTileN)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = L::kBytes + 1024;  // + slack to align the base to 1024 bytes
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(tc::gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + tc::kTileN - 1) / tc::kTileN),
+                       static_cast<unsigned>((M + T - 1) / T));
+    cfg.blockDim = dim3(tc::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc::gemm_kernel<T>, tx, tcodes, scales, y, static_cast<int>(M),
+                              static_cast<int>(N), static_cast<int>(K), 0xFFFFFFFFu, 0x10000u);
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y, int64_t M,
+                      int64_t N, int64_t K, cudaStream_t stream) {
+    if (M <= 16) return launch_tc_t<16>(x, codes, scales, y, M, N, K, stream);
+    if (M <= 32) return launch_tc_t<32>(x, codes, scales, y, M, N, K, stream);
+    if (M <= 64) return launch_tc_t<64>(x, codes, scales, y, M, N, K, stream);
+    if (M <= 128) return launch_tc_t<128>(x, codes, scales, y, M, N, K, stream);
+    return launch_tc_t<256>(x, codes, scales, y, M, N, K, stream);
+}
+
+cudaError_t read_and_clear_error(int* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
+    *code = v;
+    return e;
+}
 
 // Largest K the register-resident layout covers: kMaxWarps slices of 32 (one lane per group) or 16
 // groups (two lanes per group).
@@ -342,7 +446,7 @@ cudaError_t ensure_tables(int device, cudaStream_t stream) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_tables.mu);
     if (g_tables.ready[device]) return cudaSuccess;
-    build_vtab_kernel<<<4, 256, 0, stream>>>();
+    build_vtab_kernel<<<8, 256, 0, stream>>>();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // One-time wait so that later calls on any stream see the table.

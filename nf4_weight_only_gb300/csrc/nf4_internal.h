@@ -17,6 +17,13 @@ constexpr int kGemvMaxTokens = 4;
 cudaError_t launch_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
                         int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t stream);
 
+// tcgen05 tensor-core GEMM for M >= kTcMinTokens.
+constexpr int kTcMinTokens = 5;
+cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+// Device error word of the tensor-core path (nonzero after a bounded pipeline wait timed out).
+cudaError_t read_and_clear_error(int* code);
+
 // Per-device constant table used by the GEMV (built once per device, stream-ordered).
 cudaError_t ensure_tables(int device, cudaStream_t stream);
 

@@ -25,7 +25,8 @@ def header_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = header_functions()
-    assert {"nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_status_str", "nf4_abi_version"} <= set(names)
+    assert {"nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_check_device_error", "nf4_status_str",
+            "nf4_abi_version"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in include/nf4.h but not exported"
     import nf4_weight_only_gb300 as nf4

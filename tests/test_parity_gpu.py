@@ -235,3 +235,73 @@ def test_bad_alignment_rejected_on_device_pointers(nf4):
     st = lib.nf4_linear(ctypes.c_void_p(x.data_ptr() + 2), ctypes.c_void_p(codes.data_ptr()),
                         ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(y.data_ptr()), 1, 4, 128, None)
     assert st == 3  # NF4_ERR_ALIGN
+
+
+# ------------------------------------------------------------------------------------------------
+# tensor-core path (M >= 5)
+# ------------------------------------------------------------------------------------------------
+def device_error(nf4):
+    import ctypes
+    lib = nf4.load()
+    lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.nf4_check_device_error.restype = ctypes.c_int
+    code = ctypes.c_int(-1)
+    assert lib.nf4_check_device_error(ctypes.byref(code)) == 0
+    return code.value
+
+
+@pytest.mark.parametrize("m", [5, 16, 17, 32, 33, 64, 100, 128, 129, 256, 300, 512, 513])
+def test_linear_tensor_core_tokens(nf4, o, m):
+    check_linear(nf4, o, m, 257, 1024, seed=m)
+    assert device_error(nf4) == 0
+
+
+@pytest.mark.parametrize("n,k", [(1, 64), (7, 128), (128, 64), (130, 192), (383, 2048), (256, 6144), (64, 16384)])
+def test_linear_tensor_core_shapes(nf4, o, n, k):
+    check_linear(nf4, o, 40, n, k, seed=n + k, outliers=0.01)
+    assert device_error(nf4) == 0
+
+
+def test_linear_tensor_core_prefill_sampled(nf4, o):
+    """20B-shaped prefill gate projection (6144 -> 16384) at M = 512, checked on sampled outputs."""
+    from nf4_weight_only_gb300 import synth
+    n, k, m = 16384, 6144, 512
+    w = synth.device_weights(4 * 100003, n, k, DEV, outlier_frac=0.01)
+    codes, scales = nf4.quantize(w)
+    x = synth.device_activations_bf16(99 + k, m, k, DEV)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    nf4.nf4_linear(x, codes, scales, y)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    rng = np.random.default_rng(0)
+    mi = rng.integers(0, m, 3000)
+    ni = rng.integers(0, n, 3000)
+    mi[:8] = [0, m - 1, 0, m - 1, 255, 256, 511, 7]
+    ni[:8] = [0, 0, n - 1, n - 1, 127, 128, 16383, 8191]
+    c_h = codes.cpu().numpy()
+    s_h = scales.cpu().view(torch.int16).numpy().view(np.uint16)
+    x_h = dev_to_bits(x)
+    y64, mag = o.linear_entries(x_h, c_h, s_h, mi, ni)
+    ok, ratio, mask = oracle.within_tolerance(dev_to_bits(y)[mi, ni], y64, mag)
+    assert ok, f"{np.count_nonzero(~mask)} sampled outputs outside tolerance (worst {ratio:.3f})"
+
+
+def test_linear_negative_and_zero_scales(nf4, o):
+    """Scales outside what quantize writes (negative, zero, tiny subnormal) follow the same rule."""
+    from nf4_weight_only_gb300 import synth
+    rng = np.random.default_rng(5)
+    n, k = 200, 512
+    codes = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    scales = (rng.standard_normal((n, k // 64)) * 0.05).astype(np.float16)
+    scales[0, :] = 0
+    scales[1, :] = np.float16(-0.0)
+    scales[2, :] = np.float16(2.0 ** -24)
+    scales[3, :] = np.float16(65504.0)
+    sbits = scales.view(np.uint16)
+    for m in (1, 3, 9, 40):
+        x = synth.activations_bf16(m, m, k)
+        y = run_linear(nf4, x, codes, sbits)
+        y64, mag = o.linear(x, codes, sbits)
+        ok, ratio, _ = oracle.within_tolerance(y, y64, mag)
+        assert ok, (m, ratio)
+    assert device_error(nf4) == 0
