@@ -168,8 +168,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         for (int j = 0; j < kRows; j++)
             if (r_first + j < N) prefetch_l2(codes + (r_first + j) * row_bytes + k0 / 2);
     }
-    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(smem)[i] = ld_ca_v4(&g_vtab[i]);
+    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x)  // all copies in flight at once
+        cp_async16(smem + 16 * i, &g_vtab[i]);
+    cp_async_commit();
     pdl_wait();
 
     uint32_t xr[MT][SH::WPL / 2];
@@ -185,7 +186,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             xr[t][4 * i + 3] = v.w;
         }
     }
-    __syncthreads();  // V table ready
 
     // Enqueue the copies of this warp's t-th row quad into ring stage t % kStages (one commit group
     // per quad, empty past the end so that group counting stays uniform).
@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
 #pragma unroll
     for (int t = 0; t < kStages - 1; t++) issue(t);
+    cp_async_wait<kStages - 1>();  // the V table group (the oldest) has landed
+    __syncthreads();
 
     for (int64_t t = 0; t < my_blocks; t++) {
         issue(t + kStages - 1);

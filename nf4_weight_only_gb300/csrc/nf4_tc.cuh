@@ -171,8 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < 4096; i += kThreads)
-        reinterpret_cast<uint4*>(smem + L::kVtab)[i] = ld_ca_v4(&g_vtab[i]);
+    for (int i = threadIdx.x; i < 4096; i += kThreads)  // all copies in flight at once
+        cp_async16(smem + L::kVtab + 16 * i, &g_vtab[i]);
+    cp_async_commit();
+    cp_async_wait<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -240,11 +242,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n = n0 + r;
         const bool valid = n < N;
         const uint16_t* srow = scales + n * G;
-        uint16_t sc_next = valid ? ld_nc_u16(srow) : static_cast<uint16_t>(0);
-        for (int kb = 0; kb < KB; kb++) {
+        // Scales of the next kScaleAhead groups are kept in flight in a register ring (indexed by
+        // kb % kScaleAhead after unrolling, so it stays in registers).
+        constexpr int kScaleAhead = 4;
+        uint16_t ring[kScaleAhead];
+#pragma unroll
+        for (int u = 0; u < kScaleAhead; u++) ring[u] = (valid && u < KB) ? ld_nc_u16(srow + u) : uint16_t(0);
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += kScaleAhead) {
+#pragma unroll
+        for (int u = 0; u < kScaleAhead; u++) {
+            const int kb = kb0 + u;
+            if (kb >= KB) break;
             const int s = kb % kStages;
-            const uint16_t sc = sc_next;
-            if (valid && kb + 1 < KB) sc_next = ld_nc_u16(srow + kb + 1);
+            const uint16_t sc = ring[u];
+            if (valid && kb + kScaleAhead < KB) ring[u] = ld_nc_u16(srow + kb + kScaleAhead);
             const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(bar_loaded + 8 * s, (kb / kStages) & 1, deadline));
             if (!got) {
                 record_error(3);
@@ -285,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_full + 8 * s);
+        }
         }
         // ---------------- epilogue ----------------
         if (ok && !__all_sync(0xFFFFFFFFu, mbar_wait(bar_accum, 0, deadline))) {
