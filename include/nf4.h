@@ -91,6 +91,26 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * nf4_linear_grouped - several linears that read the same x, y_i = x * w_hat_i^T for i < count
+ * (for instance the q, k and v projections, or the gate and up projections, of one decoder layer;
+ * the deep-fold README's execution-path table runs decode as GEMVs over such linears).  For M <= 4
+ * the linears run as one CUDA-core launch over their concatenated rows; for larger M they run one
+ * tensor-core GEMM after another on `stream`.  Results equal those of count nf4_linear calls.
+ *   x        in   bf16 bits [M][K], shared by all linears
+ *   count    1 .. 8
+ *   codes    host array of count device pointers; codes[i]: uint8 [Ns[i]][K/2]
+ *   scales   host array of count device pointers; scales[i]: fp16 bits [Ns[i]][K/64]
+ *   ys       host array of count device pointers; ys[i]: bf16 bits [M][Ns[i]]; no y may overlap x,
+ *            any codes or scales, or another y
+ *   Ns       host array of count row counts (each >= 0, sum <= 2^31 - 1); empty linears are skipped
+ * The host arrays are read before the call returns.  Errors as for nf4_linear (count outside
+ * 1..8 gives NF4_ERR_SHAPE).
+ */
+nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count, const uint8_t* const* codes,
+                              const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns,
+                              cudaStream_t stream);
+
+/*
  * nf4_check_device_error - diagnostics: read and clear the device-side error word of the current
  * device.  The tensor-core path bounds every pipeline wait (about one second); a wait that runs
  * out records a nonzero code there, and the kernel drains and exits instead of hanging.  *code

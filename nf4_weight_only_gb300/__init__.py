@@ -22,8 +22,8 @@ STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_
                 4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA"}
 
 # Every symbol include/nf4.h declares.
-EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_check_device_error", "nf4_status_str",
-            "nf4_abi_version")
+EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_check_device_error",
+            "nf4_status_str", "nf4_abi_version")
 
 
 class NF4Error(RuntimeError):
@@ -52,6 +52,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_dequant.restype = ci
     lib.nf4_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     lib.nf4_linear.restype = ci
+    lib.nf4_linear_grouped.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp, vp]
+    lib.nf4_linear_grouped.restype = ci
     lib.nf4_status_str.argtypes = [ci]
     lib.nf4_status_str.restype = ctypes.c_char_p
     lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -108,6 +110,22 @@ def nf4_linear(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: to
     n = codes.shape[0]
     _check(load().nf4_linear(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
            "nf4_linear")
+
+
+def nf4_linear_grouped(x: torch.Tensor, codes, scales, ys, stream=None) -> None:
+    """ys[i][M, N_i] = x[M, K] * w_hat_i^T for the lists codes, scales, ys (same length, <= 8)."""
+    m, k = x.shape
+    n = len(codes)
+    if not (len(scales) == len(ys) == n):
+        raise ValueError("codes, scales and ys must have the same length")
+    arr = ctypes.c_void_p * n
+    c_arr = arr(*[_ptr(c).value for c in codes])
+    s_arr = arr(*[_ptr(s).value for s in scales])
+    y_arr = arr(*[_ptr(y).value for y in ys])
+    ns = (ctypes.c_int64 * n)(*[c.shape[0] for c in codes])
+    _check(load().nf4_linear_grouped(_ptr(x), m, k, n, ctypes.cast(c_arr, ctypes.c_void_p),
+                                     ctypes.cast(s_arr, ctypes.c_void_p), ctypes.cast(y_arr, ctypes.c_void_p),
+                                     ctypes.cast(ns, ctypes.c_void_p), _stream(stream)), "nf4_linear_grouped")
 
 
 def nf4_check_device_error() -> int:

@@ -81,6 +81,69 @@ const char* nf4_status_str(nf4_status status) {
 
 int nf4_abi_version(void) { return NF4_ABI_VERSION; }
 
+nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count, const uint8_t* const* codes,
+                              const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns,
+                              cudaStream_t stream) {
+    if (count < 1 || count > nf4::kMaxGroupedLinears) return NF4_ERR_SHAPE;
+    if (!codes || !scales || !ys || !Ns) return NF4_ERR_NULL;
+    if (M < 0 || M > kMaxDim) return NF4_ERR_SHAPE;
+    nf4_status st = check_k(K);
+    if (st != NF4_OK) return st;
+    int64_t rows = 0;
+    for (int i = 0; i < count; i++) {
+        if (Ns[i] < 0 || Ns[i] > kMaxDim) return NF4_ERR_SHAPE;
+        rows += Ns[i];
+    }
+    if (rows > kMaxDim) return NF4_ERR_SHAPE;
+    if (M == 0 || rows == 0) return NF4_OK;
+    if (!x) return NF4_ERR_NULL;
+    if (!aligned16(x)) return NF4_ERR_ALIGN;
+    const int64_t xb = M * K * 2;
+    for (int i = 0; i < count; i++) {
+        if (Ns[i] == 0) continue;
+        if (!codes[i] || !scales[i] || !ys[i]) return NF4_ERR_NULL;
+        if (!aligned16(codes[i]) || !aligned16(scales[i]) || !aligned16(ys[i])) return NF4_ERR_ALIGN;
+    }
+    for (int i = 0; i < count; i++) {
+        if (Ns[i] == 0) continue;
+        const int64_t yb = M * Ns[i] * 2;
+        if (overlap(ys[i], yb, x, xb)) return NF4_ERR_ALIAS;
+        for (int j = 0; j < count; j++) {
+            if (Ns[j] == 0) continue;
+            const int64_t cb = Ns[j] * K / 2, sb = Ns[j] * (K / NF4_GROUP_SIZE) * 2;
+            if (overlap(ys[i], yb, codes[j], cb) || overlap(ys[i], yb, scales[j], sb)) return NF4_ERR_ALIAS;
+            if (j != i && overlap(ys[i], yb, ys[j], M * Ns[j] * 2)) return NF4_ERR_ALIAS;
+        }
+    }
+    if (M < nf4::kTcMinTokens && K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
+    if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
+    if (M < nf4::kTcMinTokens) {
+        // drop empty problems, keep the order
+        const uint8_t* c[nf4::kMaxGroupedLinears];
+        const uint16_t* sc[nf4::kMaxGroupedLinears];
+        uint16_t* yy[nf4::kMaxGroupedLinears];
+        int64_t nn[nf4::kMaxGroupedLinears];
+        int k = 0;
+        for (int i = 0; i < count; i++)
+            if (Ns[i] > 0) {
+                c[k] = codes[i];
+                sc[k] = scales[i];
+                yy[k] = ys[i];
+                nn[k] = Ns[i];
+                k++;
+            }
+        return from_cuda(nf4::launch_gemv_grouped(x, k, c, sc, yy, nn, M, K, sms, stream));
+    }
+    for (int i = 0; i < count; i++) {
+        if (Ns[i] == 0) continue;
+        if ((st = from_cuda(nf4::launch_tc(x, codes[i], scales[i], ys[i], M, Ns[i], K, stream))) != NF4_OK)
+            return st;
+    }
+    return NF4_OK;
+}
+
 nf4_status nf4_check_device_error(int* code) {
     if (!code) return NF4_ERR_NULL;
     *code = 0;

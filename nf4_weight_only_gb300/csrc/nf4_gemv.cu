@@ -111,6 +111,24 @@ __device__ __forceinline__ float reduce_transposed(float (&v)[V], int lane) {
 
 __host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
 
+// Up to kMaxGroup linears that share x and K, run as one launch over their concatenated rows.
+constexpr int kMaxGroup = 8;
+struct GemvProblems {
+    const uint8_t* codes[kMaxGroup];
+    const uint16_t* scales[kMaxGroup];
+    uint16_t* y[kMaxGroup];
+    int row0[kMaxGroup + 1];  // first concatenated row of each problem; row0[count] = total rows
+    int count;
+};
+
+// Problem holding concatenated row r (rows are sorted, count is small).
+__device__ __forceinline__ int problem_of(const GemvProblems& P, int64_t r) {
+    int p = 0;
+    for (int i = 1; i < P.count; i++)
+        if (r >= P.row0[i]) p = i;
+    return p;
+}
+
 template <int MT, int LPG>
 struct GemvShape {
     static constexpr int WPL = kGroup / LPG;   // weights per lane per row
@@ -128,13 +146,13 @@ struct GemvShape {
 // two [S][Q*kRows][MT] slice-partial buffers when S > 1.
 template <int MT, int LPG>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
-    gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes,
-                const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int N, int K, int S, int Q,
+    gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K, int S, int Q,
                 uint32_t m1, uint32_t p16) {
     using SH = GemvShape<MT, LPG>;
     constexpr int V = pow2_ceil(kRows * MT);
     extern __shared__ __align__(16) uint8_t smem[];
 
+    const int N = P.row0[P.count];  // concatenated rows
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -154,8 +172,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         blockIdx.x < nblocks ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const uint32_t row_bytes = static_cast<uint32_t>(K / 2);
     const uint32_t row_sbytes = static_cast<uint32_t>(G * 2);
-    const int64_t scale_bytes = static_cast<int64_t>(N) * row_sbytes;
-    const uint8_t* scale_base = reinterpret_cast<const uint8_t*>(scales);
     const int64_t rstep = static_cast<int64_t>(gridDim.x) * rows_per_block;
 
     // Let the next kernel in the stream launch, warm L2 with this warp's first rows (a prefetch
@@ -166,7 +182,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     if (my_blocks > 0 && active) {
 #pragma unroll
         for (int j = 0; j < kRows; j++)
-            if (r_first + j < N) prefetch_l2(codes + (r_first + j) * row_bytes + k0 / 2);
+            if (r_first + j < N) {
+                const int pp = problem_of(P, r_first + j);
+                prefetch_l2(P.codes[pp] + (r_first + j - P.row0[pp]) * row_bytes + k0 / 2);
+            }
     }
     for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x)  // all copies in flight at once
         cp_async16(smem + 16 * i, &g_vtab[i]);
@@ -193,26 +212,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         if (t < my_blocks) {
             uint8_t* st = ring + static_cast<int>(t % kStages) * SH::STAGE;
             const int64_t r0 = r_first + t * rstep;
-            const uint8_t* src = codes + r0 * row_bytes + k0 / 2;
-            int64_t sfirst = (r0 * G + s * SH::GPW) * 2;  // first scale byte of the row's slice
 #pragma unroll
             for (int j = 0; j < kRows; j++) {
-                if (r0 + j < N) {
+                const int64_t r = r0 + j;
+                if (r < N) {
+                    const int pp = problem_of(P, r);
+                    const int64_t lr = r - P.row0[pp];  // row inside problem pp
                     if (active) {
+                        const uint8_t* src = P.codes[pp] + lr * row_bytes + k0 / 2;
 #pragma unroll
                         for (int c = 0; c < SH::CHUNKS; c++)
                             cp_async16(st + ((j * 32 + lane) * SH::CHUNKS + (c ^ sw)) * 16, src + 16 * c);
                     }
-                    const int64_t a = sfirst & ~static_cast<int64_t>(15);
-                    const int64_t chunk = a + 16 * lane;
+                    // scale window of this row's slice: [first byte rounded down to 16, last byte]
+                    const int64_t sfirst = (lr * G + s * SH::GPW) * 2;
+                    const int64_t chunk = (sfirst & ~static_cast<int64_t>(15)) + 16 * lane;
                     if (chunk < sfirst + 2 * (g_hi - s * SH::GPW)) {
-                        const int64_t left = scale_bytes - chunk;
-                        cp_async16(st + SH::STAGE_CODES + j * SH::SWIN + 16 * lane, scale_base + chunk,
+                        const int64_t left =
+                            static_cast<int64_t>(P.row0[pp + 1] - P.row0[pp]) * row_sbytes - chunk;
+                        cp_async16(st + SH::STAGE_CODES + j * SH::SWIN + 16 * lane,
+                                   reinterpret_cast<const uint8_t*>(P.scales[pp]) + chunk,
                                    static_cast<uint32_t>(left < 16 ? left : 16));
                     }
                 }
-                src += row_bytes;
-                sfirst += row_sbytes;
             }
         }
         cp_async_commit();
@@ -231,9 +253,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const int64_t r0 = r_first + t * rstep;
         // Row j's scale window starts at its first scale byte rounded down to 16; the lane's scale
         // sits (first byte mod 16) + 2 * (g - first group) bytes into it.
-        const int f0lo = static_cast<int>(((r0 * G + s * SH::GPW) * 2) & 15);
         const int goff = 2 * (g - s * SH::GPW);
-        const int rlo = static_cast<int>(row_sbytes & 15u);
         float part[V];
 #pragma unroll
         for (int i = 0; i < V; i++) part[i] = 0.0f;
@@ -242,7 +262,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             if (r0 + j >= N) continue;  // warp-uniform
             uint32_t sc = 0;
             if (active) {
-                const int off = ((f0lo + j * rlo) & 15) + goff;
+                const int pp = problem_of(P, r0 + j);
+                const uint32_t lr = static_cast<uint32_t>(r0 + j - P.row0[pp]);
+                const int off = static_cast<int>(((lr * static_cast<uint32_t>(G) + s * SH::GPW) * 2u) & 15u) + goff;
                 sc = *reinterpret_cast<const uint16_t*>(st + SH::STAGE_CODES + j * SH::SWIN + off);
             }
             const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
@@ -279,7 +301,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const bool writer = (lane % lanes_per_value) == 0 && idx < kRows * MT;
         const int j = idx / MT, tt = idx % MT;
         if (S == 1) {
-            if (writer && r0 + j < N) y[static_cast<int64_t>(tt) * N + r0 + j] = bf16_bits(total);
+            if (writer && r0 + j < N) {
+                const int pp = problem_of(P, r0 + j);
+                const int np = P.row0[pp + 1] - P.row0[pp];
+                P.y[pp][static_cast<int64_t>(tt) * np + (r0 + j - P.row0[pp])] = bf16_bits(total);
+            }
         } else {
             const int64_t rb = blockIdx.x + t * gridDim.x;
             float* buf = red + (t & 1) * S * rows_per_block * MT;
@@ -289,7 +315,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 const int64_t r = rb * rows_per_block + i / MT;
                 float acc = 0.0f;
                 for (int ss = 0; ss < S; ss++) acc += buf[ss * rows_per_block * MT + i];
-                if (r < N) y[static_cast<int64_t>(i % MT) * N + r] = bf16_bits(acc);
+                if (r < N) {
+                    const int pp = problem_of(P, r);
+                    const int np = P.row0[pp + 1] - P.row0[pp];
+                    P.y[pp][static_cast<int64_t>(i % MT) * np + (r - P.row0[pp])] = bf16_bits(acc);
+                }
             }
         }
     }
@@ -303,8 +333,8 @@ struct TableState {
 TableState g_tables;
 
 template <int MT, int LPG>
-cudaError_t launch_gemv_t(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
-                          int64_t N, int64_t K, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
+    const int64_t N = P.row0[P.count];
     using SH = GemvShape<MT, LPG>;
     const int G = static_cast<int>(K / kGroup);
     const int S = (G + SH::GPW - 1) / SH::GPW;
@@ -339,8 +369,8 @@ cudaError_t launch_gemv_t(const uint16_t* x, const uint8_t* codes, const uint16_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, codes, scales, y, static_cast<int>(N),
-                              static_cast<int>(K), S, Q, 0xFFFFFFFFu, 0x10000u);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, P, static_cast<int>(K), S, Q, 0xFFFFFFFFu,
+                              0x10000u);
 }
 
 }  // namespace
@@ -458,15 +488,35 @@ cudaError_t ensure_tables(int device, cudaStream_t stream) {
     return cudaSuccess;
 }
 
-cudaError_t launch_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
-                        int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* const* codes,
+                                const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns, int64_t M,
+                                int64_t K, int num_sms, cudaStream_t stream) {
+    if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
+    GemvProblems P = {};
+    P.count = count;
+    int64_t rows = 0;
+    for (int i = 0; i < count; i++) {
+        P.codes[i] = codes[i];
+        P.scales[i] = scales[i];
+        P.y[i] = ys[i];
+        P.row0[i] = static_cast<int>(rows);
+        rows += Ns[i];
+    }
+    if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    P.row0[count] = static_cast<int>(rows);
+    for (int i = count + 1; i <= kMaxGroup; i++) P.row0[i] = P.row0[count];
     switch (M) {
-        case 1: return launch_gemv_t<1, 1>(x, codes, scales, y, N, K, num_sms, stream);
-        case 2: return launch_gemv_t<2, 2>(x, codes, scales, y, N, K, num_sms, stream);
-        case 3: return launch_gemv_t<3, 2>(x, codes, scales, y, N, K, num_sms, stream);
-        case 4: return launch_gemv_t<4, 2>(x, codes, scales, y, N, K, num_sms, stream);
+        case 1: return launch_gemv_t<1, 1>(x, P, K, num_sms, stream);
+        case 2: return launch_gemv_t<2, 2>(x, P, K, num_sms, stream);
+        case 3: return launch_gemv_t<3, 2>(x, P, K, num_sms, stream);
+        case 4: return launch_gemv_t<4, 2>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
+                        int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t stream) {
+    return launch_gemv_grouped(x, 1, &codes, &scales, &y, &N, M, K, num_sms, stream);
 }
 
 }  // namespace nf4

@@ -17,6 +17,12 @@ constexpr int kGemvMaxTokens = 4;
 cudaError_t launch_gemv(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
                         int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t stream);
 
+// The same for up to kMaxGroupedLinears linears sharing x and K (concatenated rows, one launch).
+constexpr int kMaxGroupedLinears = 8;
+cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* const* codes,
+                                const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns, int64_t M,
+                                int64_t K, int num_sms, cudaStream_t stream);
+
 // tcgen05 tensor-core GEMM for M >= kTcMinTokens.
 constexpr int kTcMinTokens = 5;
 cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,

@@ -25,8 +25,8 @@ def header_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = header_functions()
-    assert {"nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_check_device_error", "nf4_status_str",
-            "nf4_abi_version"} <= set(names)
+    assert {"nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_check_device_error",
+            "nf4_status_str", "nf4_abi_version"} <= set(names)
     for name in names:
         assert hasattr(lib, name), f"{name} declared in include/nf4.h but not exported"
     import nf4_weight_only_gb300 as nf4
@@ -107,3 +107,22 @@ def test_binding_raises_without_library(tmp_path):
     import nf4_weight_only_gb300 as nf4
     with pytest.raises(RuntimeError, match="missing"):
         nf4.load(str(tmp_path / "nope.so"))
+
+
+def test_grouped_validation(lib):
+    arr = ctypes.c_void_p * 2
+    ns = (ctypes.c_int64 * 2)(16, 8)
+    g = lib.nf4_linear_grouped
+    c2 = arr(B, B + 4096)
+    s2 = arr(C, C + 4096)
+    y2 = arr(D, D + 4096)
+    args = lambda x, m, k, cnt, c, s, y, n: g(vp(x), m, k, cnt, ctypes.cast(c, vp), ctypes.cast(s, vp),
+                                             ctypes.cast(y, vp), ctypes.cast(n, vp), None)
+    assert args(A, 1, 64, 0, c2, s2, y2, ns) == 2          # count outside 1..8
+    assert args(A, 1, 64, 9, c2, s2, y2, ns) == 2
+    assert args(A, 1, 100, 2, c2, s2, y2, ns) == 2         # K not a multiple of 64
+    assert g(vp(A), 1, 64, 2, None, ctypes.cast(s2, vp), ctypes.cast(y2, vp), ctypes.cast(ns, vp), None) == 1
+    assert args(A + 2, 1, 64, 2, c2, s2, y2, ns) == 3      # misaligned x
+    assert args(A, 1, 64, 2, c2, s2, arr(D, D + 16), ns) == 4  # y0 (32 bytes) and y1 overlap
+    assert args(A, 1, 64, 2, c2, s2, arr(D, B + 16), ns) == 4  # y1 inside codes[0]
+    assert args(A, 0, 64, 2, c2, s2, y2, ns) == 0          # empty

@@ -305,3 +305,34 @@ def test_linear_negative_and_zero_scales(nf4, o):
         ok, ratio, _ = oracle.within_tolerance(y, y64, mag)
         assert ok, (m, ratio)
     assert device_error(nf4) == 0
+
+
+# ------------------------------------------------------------------------------------------------
+# grouped linears sharing x
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("m", [1, 3, 4, 7])
+def test_linear_grouped_matches_single(nf4, o, m):
+    """q, k and v of a 2048-wide layer (plus a ragged fourth) in one call equal separate calls and
+    meet the oracle bound."""
+    from nf4_weight_only_gb300 import synth
+    k = 2048
+    ns = [2048, 256, 256, 37]
+    x = synth.activations_bf16(50 + m, m, k)
+    xd = bf16_to_dev(x)
+    mats = []
+    for i, n in enumerate(ns):
+        w = synth.weights(60 + i, n, k)
+        c, s = o.quantize(w)
+        mats.append((c, s, torch.from_numpy(c).to(DEV),
+                     torch.from_numpy(s.view(np.int16)).view(torch.float16).to(DEV)))
+    ys = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for n in ns]
+    nf4.nf4_linear_grouped(xd, [t[2] for t in mats], [t[3] for t in mats], ys)
+    torch.cuda.synchronize()
+    for (c, s, cd, sd), y in zip(mats, ys):
+        single = torch.empty_like(y)
+        nf4.nf4_linear(xd, cd, sd, single)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), single.view(torch.int16))
+        y64, mag = o.linear(x, c, s, nthreads=16)
+        ok, ratio, _ = oracle.within_tolerance(dev_to_bits(y), y64, mag)
+        assert ok, ratio
