@@ -32,9 +32,7 @@
 namespace nf4 {
 namespace {
 
-constexpr int kRows = 4;       // rows per warp iteration
 constexpr int kMaxWarps = 16;  // warps per CTA (slices x row lanes)
-constexpr int kStages = 2;     // per-warp shared-memory ring depth (row quads in flight)
 constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
 // V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
@@ -129,26 +127,30 @@ __device__ __forceinline__ int problem_of(const GemvProblems& P, int64_t r) {
     return p;
 }
 
-template <int MT, int LPG>
+// MT tokens, LPG lanes per group, R rows per warp iteration, ST ring stages per warp.
+template <int MT, int LPG, int R, int ST>
 struct GemvShape {
     static constexpr int WPL = kGroup / LPG;   // weights per lane per row
     static constexpr int CB = WPL / 2;         // code bytes per lane per row
     static constexpr int CHUNKS = CB / 16;     // 16-byte copies per lane per row
     static constexpr int GPW = 32 / LPG;       // groups per warp slice
     static constexpr int SWIN = 2 * GPW + 16;  // bytes of a row's 16-byte-aligned scale window
-    static constexpr int STAGE_CODES = kRows * 32 * CB;
-    static constexpr int STAGE = STAGE_CODES + kRows * SWIN;
-    static constexpr int WARP_SMEM = kStages * STAGE;
+    static constexpr int STAGE_CODES = R * 32 * CB;
+    static constexpr int STAGE = STAGE_CODES + R * SWIN;
+    static constexpr int WARP_SMEM = ST * STAGE;
 };
 
-// MT tokens; LPG lanes per 64-weight group (1 or 2).  Shared memory: the V table (32 KB), then one
-// private ring of kStages row quads per warp (codes and scale windows, filled with cp.async), then
-// two [S][Q*kRows][MT] slice-partial buffers when S > 1.
-template <int MT, int LPG>
+// MT tokens; LPG lanes per 64-weight group (1 or 2); R rows per warp iteration (4 for large
+// matrices, 1 for small ones so that more warps share the work); ST stages in each warp's ring.
+// Shared memory: the V table (32 KB), then one private ring of ST row batches per warp (codes and
+// scale windows, filled with cp.async), then two [S][Q*R][MT] slice-partial buffers when S > 1.
+template <int MT, int LPG, int R, int ST>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K, int S, int Q,
                 uint32_t m1, uint32_t p16) {
-    using SH = GemvShape<MT, LPG>;
+    using SH = GemvShape<MT, LPG, R, ST>;
+    constexpr int kRows = R;
+    constexpr int kStages = ST;
     constexpr int V = pow2_ceil(kRows * MT);
     extern __shared__ __align__(16) uint8_t smem[];
 
@@ -218,11 +220,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 if (r < N) {
                     const int pp = problem_of(P, r);
                     const int64_t lr = r - P.row0[pp];  // row inside problem pp
-                    if (active) {
-                        const uint8_t* src = P.codes[pp] + lr * row_bytes + k0 / 2;
+                    // Consecutive lanes copy consecutive 16-byte chunks of the slice's row (full
+                    // sectors per instruction); chunk q belongs to compute lane q / CHUNKS and lands
+                    // in that lane's (swizzled) slot.
+                    const uint8_t* src = P.codes[pp] + lr * row_bytes + s * SH::GPW * (kGroup / 2);
 #pragma unroll
-                        for (int c = 0; c < SH::CHUNKS; c++)
-                            cp_async16(st + ((j * 32 + lane) * SH::CHUNKS + (c ^ sw)) * 16, src + 16 * c);
+                    for (int c = 0; c < SH::CHUNKS; c++) {
+                        const int q = lane + 32 * c;
+                        const int lq = q / SH::CHUNKS, hq = q % SH::CHUNKS;
+                        const int swq = LPG == 1 ? ((lq >> 2) & 1) : 0;
+                        if (s * SH::GPW + lq / LPG < G)
+                            cp_async16(st + ((j * 32 + lq) * SH::CHUNKS + (hq ^ swq)) * 16, src + 16 * q);
                     }
                     // scale window of this row's slice: [first byte rounded down to 16, last byte]
                     const int64_t sfirst = (lr * G + s * SH::GPW) * 2;
@@ -332,10 +340,11 @@ struct TableState {
 };
 TableState g_tables;
 
-template <int MT, int LPG>
+template <int MT, int LPG, int R, int ST>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
     const int64_t N = P.row0[P.count];
-    using SH = GemvShape<MT, LPG>;
+    using SH = GemvShape<MT, LPG, R, ST>;
+    constexpr int kRows = R;
     const int G = static_cast<int>(K / kGroup);
     const int S = (G + SH::GPW - 1) / SH::GPW;
     // Row lanes per slice: enough CTAs to cover the SMs when N is small, at most kMaxWarps warps.
@@ -350,15 +359,17 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     const int grid = static_cast<int>(blocks_needed < num_sms ? blocks_needed : num_sms);
     const size_t smem = kVtabBytes + static_cast<size_t>(warps) * SH::WARP_SMEM +
                         (S > 1 ? 2 * static_cast<size_t>(S) * rows_per_block * MT * sizeof(float) : 0);
-    static bool attr_set = false;  // the largest request is set once per process
-    if (!attr_set) {
+    static std::once_flag attr_once[64];  // the largest request, set once per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
         const size_t max_smem = kVtabBytes + static_cast<size_t>(kMaxWarps) * SH::WARP_SMEM +
                                 2 * static_cast<size_t>(kMaxWarps) * kRows * MT * sizeof(float);
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT, LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(max_smem));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG, R, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(max_smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(32 * warps);
@@ -369,7 +380,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, P, static_cast<int>(K), S, Q, 0xFFFFFFFFu,
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, R, ST>, x, P, static_cast<int>(K), S, Q, 0xFFFFFFFFu,
                               0x10000u);
 }
 
@@ -505,11 +516,19 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
     if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
     P.row0[count] = static_cast<int>(rows);
     for (int i = count + 1; i <= kMaxGroup; i++) P.row0[i] = P.row0[count];
+    // HBM latency under load is a few microseconds, so each SM needs on the order of 100 KB of
+    // copies in flight: large matrices use 2 rows per warp iteration and a 5-deep ring (4 batches
+    // in flight per warp), smaller ones 1 row and an 8-deep ring so that many warps share the rows.
+    const bool large = rows >= static_cast<int64_t>(2) * kMaxWarps * num_sms;
     switch (M) {
-        case 1: return launch_gemv_t<1, 1>(x, P, K, num_sms, stream);
-        case 2: return launch_gemv_t<2, 2>(x, P, K, num_sms, stream);
-        case 3: return launch_gemv_t<3, 2>(x, P, K, num_sms, stream);
-        case 4: return launch_gemv_t<4, 2>(x, P, K, num_sms, stream);
+        case 1: return large ? launch_gemv_t<1, 1, 2, 5>(x, P, K, num_sms, stream)
+                             : launch_gemv_t<1, 1, 1, 8>(x, P, K, num_sms, stream);
+        case 2: return large ? launch_gemv_t<2, 2, 4, 2>(x, P, K, num_sms, stream)
+                             : launch_gemv_t<2, 2, 1, 4>(x, P, K, num_sms, stream);
+        case 3: return large ? launch_gemv_t<3, 2, 4, 2>(x, P, K, num_sms, stream)
+                             : launch_gemv_t<3, 2, 1, 4>(x, P, K, num_sms, stream);
+        case 4: return large ? launch_gemv_t<4, 2, 4, 2>(x, P, K, num_sms, stream)
+                             : launch_gemv_t<4, 2, 1, 4>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
