@@ -32,7 +32,7 @@
 namespace nf4 {
 namespace {
 
-constexpr int kMaxWarps = 16;  // warps per CTA (slices x row lanes)
+constexpr int kMaxWarps = 16;  // consumer warps per CTA (slices x row lanes)
 constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
 // V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
@@ -127,211 +127,254 @@ __device__ __forceinline__ int problem_of(const GemvProblems& P, int64_t r) {
     return p;
 }
 
-// MT tokens, LPG lanes per group, R rows per warp iteration, ST ring stages per warp.
-template <int MT, int LPG, int R, int ST>
-struct GemvShape {
-    static constexpr int WPL = kGroup / LPG;   // weights per lane per row
-    static constexpr int CB = WPL / 2;         // code bytes per lane per row
-    static constexpr int CHUNKS = CB / 16;     // 16-byte copies per lane per row
-    static constexpr int GPW = 32 / LPG;       // groups per warp slice
-    static constexpr int SWIN = 2 * GPW + 16;  // bytes of a row's 16-byte-aligned scale window
-    static constexpr int STAGE_CODES = R * 32 * CB;
-    static constexpr int STAGE = STAGE_CODES + R * SWIN;
-    static constexpr int WARP_SMEM = ST * STAGE;
+// Error word of the bounded pipeline waits of both kernels in this translation unit.
+__device__ int g_tc_error;
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_tc_error, 0, code); }
+
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz: a wait this long means a bug
+
+// Per-row metadata the producer writes next to each row's data.
+struct RowMeta {
+    int problem;     // index into GemvProblems
+    int local_row;   // row inside that problem
+    int scale_off;   // byte offset of the row's first scale inside its 16-byte-aligned window
+    int valid;       // row < total rows
 };
 
-// MT tokens; LPG lanes per 64-weight group (1 or 2); R rows per warp iteration (4 for large
-// matrices, 1 for small ones so that more warps share the work); ST stages in each warp's ring.
-// Shared memory: the V table (32 KB), then one private ring of ST row batches per warp (codes and
-// scale windows, filled with cp.async), then two [S][Q*R][MT] slice-partial buffers when S > 1.
-template <int MT, int LPG, int R, int ST>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
-    gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K, int S, int Q,
-                uint32_t m1, uint32_t p16) {
-    using SH = GemvShape<MT, LPG, R, ST>;
-    constexpr int kRows = R;
-    constexpr int kStages = ST;
-    constexpr int V = pow2_ceil(kRows * MT);
+// Launch-time layout of one ring stage (host and device agree on it).
+struct GemvLayout {
+    int S, Q, R;         // K-slices, row lanes per slice, rows per consumer warp per block
+    int RB;              // rows per block = Q * R
+    int ST;              // ring stages
+    int row_code_bytes;  // K / 2: one row's codes, copied as they lie in memory
+    int swin;            // bytes of one row's scale window (multiple of 16)
+    int stage_bytes;     // RB * (row_code_bytes + swin) + RB * 16 (meta) + red
+    int red_off;         // offset of the [S][RB][MT] partial sums inside a stage
+    int meta_off;
+    int scales_off;
+};
+
+// Warp-specialised GEMV.  Warps 0..C-1 (C = S * Q) consume: warp c owns slice c % S and rows
+// (c / S) * R .. +R of every row block, keeps its slice of x in registers and runs the lookups and
+// fused multiply-adds.  Warp C produces: for each row block it waits until the ring stage is free,
+// copies the block's codes (16-byte chunks, consecutive lanes on consecutive chunks, each chunk
+// placed in the swizzled slot of the consumer lane that owns it), the rows' scale windows and their
+// metadata, and arms the stage's `full` barrier through cp.async.mbarrier.arrive.  With S > 1 the
+// consumers leave per-slice partial sums in the stage and consumer warp 0 adds them in slice order.
+// Every wait is bounded; after a timeout the waiting thread records an error code and stops.
+template <int MT, int LPG>
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+    gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K,
+                const GemvLayout L, uint32_t m1, uint32_t p16) {
+    constexpr int WPL = kGroup / LPG;  // weights per consumer lane per row
+    constexpr int CB = WPL / 2;        // code bytes per consumer lane per row
+    constexpr int CHUNKS = CB / 16;
+    constexpr int GPW = 32 / LPG;      // groups per slice
+    constexpr int RMAX = 2;  // rows per consumer warp per block (the launcher picks 1 or 2)
+    constexpr int V = pow2_ceil(RMAX * MT);
     extern __shared__ __align__(16) uint8_t smem[];
 
-    const int N = P.row0[P.count];  // concatenated rows
+    const int N = P.row0[P.count];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int s = warp % S, q = warp / S;
+    const int C = L.S * L.Q;
     const int G = K / kGroup;
-    const int g = s * SH::GPW + lane / LPG;
-    const bool active = g < G;
-    const int k0 = s * SH::GPW * kGroup + lane * SH::WPL;
-    const int g_hi = min(G, (s + 1) * SH::GPW);        // one past the slice's last group
-    const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;  // 16-byte chunk swizzle: conflict-free reads
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
     const uint4* vtab = reinterpret_cast<const uint4*>(smem);
-    uint8_t* ring = smem + kVtabBytes + warp * SH::WARP_SMEM;
-    float* red = reinterpret_cast<float*>(smem + kVtabBytes + nwarps * SH::WARP_SMEM);
-    const int rows_per_block = Q * kRows;
-    const int64_t nblocks = (static_cast<int64_t>(N) + rows_per_block - 1) / rows_per_block;
-    const int64_t my_blocks =
-        blockIdx.x < nblocks ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const uint32_t row_bytes = static_cast<uint32_t>(K / 2);
-    const uint32_t row_sbytes = static_cast<uint32_t>(G * 2);
-    const int64_t rstep = static_cast<int64_t>(gridDim.x) * rows_per_block;
+    uint8_t* ring = smem + kVtabBytes;
+    const uint32_t bars = sbase + kVtabBytes + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
+    const int64_t nblocks = (static_cast<int64_t>(N) + L.RB - 1) / L.RB;
+    const int64_t my_blocks = blockIdx.x < nblocks ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
-    // Let the next kernel in the stream launch, warm L2 with this warp's first rows (a prefetch
-    // never returns stale data: L2 is coherent), copy the constant table, then wait for the
-    // previous kernel's results.
     pdl_launch_dependents();
-    const int64_t r_first = static_cast<int64_t>(blockIdx.x) * rows_per_block + q * kRows;
-    if (my_blocks > 0 && active) {
-#pragma unroll
-        for (int j = 0; j < kRows; j++)
-            if (r_first + j < N) {
-                const int pp = problem_of(P, r_first + j);
-                prefetch_l2(P.codes[pp] + (r_first + j - P.row0[pp]) * row_bytes + k0 / 2);
-            }
-    }
-    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x)  // all copies in flight at once
-        cp_async16(smem + 16 * i, &g_vtab[i]);
-    cp_async_commit();
-    pdl_wait();
-
-    uint32_t xr[MT][SH::WPL / 2];
-#pragma unroll
-    for (int t = 0; t < MT; t++) {
-#pragma unroll
-        for (int i = 0; i < SH::WPL / 8; i++) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (active) v = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * K + k0 + 8 * i);
-            xr[t][4 * i + 0] = v.x;
-            xr[t][4 * i + 1] = v.y;
-            xr[t][4 * i + 2] = v.z;
-            xr[t][4 * i + 3] = v.w;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < L.ST; st++) {
+            mbar_init(bars + 8 * st, 33);  // full: per producer lane after its copies, + lane 0 after the metadata
+            mbar_init(bars + 8 * (L.ST + st), L.S > 1 ? 1 : C);     // empty
+            mbar_init(bars + 8 * (2 * L.ST + st), C);               // part: consumer partials written
         }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x) cp_async16(smem + 16 * i, &g_vtab[i]);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    const long long deadline = clock64() + kWaitCycles;
 
-    // Enqueue the copies of this warp's t-th row quad into ring stage t % kStages (one commit group
-    // per quad, empty past the end so that group counting stays uniform).
-    auto issue = [&](int64_t t) {
-        if (t < my_blocks) {
-            uint8_t* st = ring + static_cast<int>(t % kStages) * SH::STAGE;
-            const int64_t r0 = r_first + t * rstep;
-#pragma unroll
-            for (int j = 0; j < kRows; j++) {
+    if (warp == C) {
+        // ------------------------------------------------------------------ producer
+        if (my_blocks > 0) {  // warm L2 with the first block before waiting for the previous grid
+            const int64_t r = static_cast<int64_t>(blockIdx.x) * L.RB + lane;
+            if (lane < L.RB && r < N) {
+                const int pp = problem_of(P, r);
+                prefetch_l2(P.codes[pp] + (r - P.row0[pp]) * static_cast<int64_t>(K / 2));
+            }
+        }
+        pdl_wait();
+        // Lane j copies rows j, j + 32, ... of the block: each row's codes with one bulk copy
+        // (transaction bytes on the stage's `full` barrier) and its scale window with zero-filling
+        // 16-byte copies.  Every row of the block gets its metadata (valid = 0 past the end).
+        for (int64_t t = 0; t < my_blocks; t++) {
+            const int st = static_cast<int>(t % L.ST);
+            const int round = static_cast<int>(t / L.ST);
+            if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (L.ST + st), (round - 1) & 1, deadline))) {
+                record_error(11);
+                break;
+            }
+            uint8_t* stg = ring + st * L.stage_bytes;
+            const int64_t r0 = (blockIdx.x + t * gridDim.x) * static_cast<int64_t>(L.RB);
+            const int64_t valid_rows = N - r0 < L.RB ? N - r0 : L.RB;
+            if (lane == 0) mbar_expect_tx_only(bars + 8 * st, static_cast<uint32_t>(valid_rows * (K / 2)));
+            __syncwarp();
+            for (int j = lane; j < L.RB; j += 32) {
                 const int64_t r = r0 + j;
+                RowMeta meta = {0, 0, 0, 0};
                 if (r < N) {
                     const int pp = problem_of(P, r);
-                    const int64_t lr = r - P.row0[pp];  // row inside problem pp
-                    // Consecutive lanes copy consecutive 16-byte chunks of the slice's row (full
-                    // sectors per instruction); chunk q belongs to compute lane q / CHUNKS and lands
-                    // in that lane's (swizzled) slot.
-                    const uint8_t* src = P.codes[pp] + lr * row_bytes + s * SH::GPW * (kGroup / 2);
-#pragma unroll
-                    for (int c = 0; c < SH::CHUNKS; c++) {
-                        const int q = lane + 32 * c;
-                        const int lq = q / SH::CHUNKS, hq = q % SH::CHUNKS;
-                        const int swq = LPG == 1 ? ((lq >> 2) & 1) : 0;
-                        if (s * SH::GPW + lq / LPG < G)
-                            cp_async16(st + ((j * 32 + lq) * SH::CHUNKS + (hq ^ swq)) * 16, src + 16 * q);
-                    }
-                    // scale window of this row's slice: [first byte rounded down to 16, last byte]
-                    const int64_t sfirst = (lr * G + s * SH::GPW) * 2;
-                    const int64_t chunk = (sfirst & ~static_cast<int64_t>(15)) + 16 * lane;
-                    if (chunk < sfirst + 2 * (g_hi - s * SH::GPW)) {
-                        const int64_t left =
-                            static_cast<int64_t>(P.row0[pp + 1] - P.row0[pp]) * row_sbytes - chunk;
-                        cp_async16(st + SH::STAGE_CODES + j * SH::SWIN + 16 * lane,
-                                   reinterpret_cast<const uint8_t*>(P.scales[pp]) + chunk,
+                    const int64_t lr = r - P.row0[pp];
+                    bulk_copy_g2s(sbase + static_cast<uint32_t>(kVtabBytes + st * L.stage_bytes + j * L.row_code_bytes),
+                                  P.codes[pp] + lr * (K / 2), static_cast<uint32_t>(K / 2), bars + 8 * st);
+                    const int64_t sfirst = lr * G * 2;
+                    const int64_t a = sfirst & ~static_cast<int64_t>(15);
+                    const int64_t total = static_cast<int64_t>(P.row0[pp + 1] - P.row0[pp]) * G * 2;
+                    const uint8_t* sp = reinterpret_cast<const uint8_t*>(P.scales[pp]);
+                    for (int64_t c = a; c < sfirst + 2 * G; c += 16) {
+                        const int64_t left = total - c;
+                        cp_async16(stg + L.scales_off + j * L.swin + (c - a), sp + c,
                                    static_cast<uint32_t>(left < 16 ? left : 16));
                     }
+                    meta = {pp, static_cast<int>(lr), static_cast<int>(sfirst - a), 1};
                 }
+                *reinterpret_cast<RowMeta*>(stg + L.meta_off + 16 * j) = meta;
+            }
+            // full = the bulk bytes + every lane's small copies (asynchronous arrive per lane) +
+            // lane 0's release of the metadata written by the whole warp
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bars + 8 * st) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * st);
+        }
+        cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int s = warp % L.S, q = warp / L.S;
+        const int g = s * GPW + lane / LPG;
+        const bool active = g < G;
+        const int k0 = s * GPW * kGroup + lane * WPL;
+        // Lanes whose bit 2 is set read the two 16-byte halves of their 32 code bytes in the other
+        // order (no bank conflicts for eight lanes 32 bytes apart); x is loaded in the same order.
+        const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
+        pdl_wait();
+        uint32_t xr[MT][WPL / 2];
+#pragma unroll
+        for (int tt = 0; tt < MT; tt++) {
+#pragma unroll
+            for (int i = 0; i < WPL / 8; i++) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                const int isrc = i ^ (sw * (WPL / 16));  // swap the halves for swizzled lanes
+                if (active) v = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tt) * K + k0 + 8 * isrc);
+                xr[tt][4 * i + 0] = v.x;
+                xr[tt][4 * i + 1] = v.y;
+                xr[tt][4 * i + 2] = v.z;
+                xr[tt][4 * i + 3] = v.w;
             }
         }
-        cp_async_commit();
-    };
-
-#pragma unroll
-    for (int t = 0; t < kStages - 1; t++) issue(t);
-    cp_async_wait<kStages - 1>();  // the V table group (the oldest) has landed
-    __syncthreads();
-
-    for (int64_t t = 0; t < my_blocks; t++) {
-        issue(t + kStages - 1);
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint8_t* st = ring + static_cast<int>(t % kStages) * SH::STAGE;
-        const int64_t r0 = r_first + t * rstep;
-        // Row j's scale window starts at its first scale byte rounded down to 16; the lane's scale
-        // sits (first byte mod 16) + 2 * (g - first group) bytes into it.
-        const int goff = 2 * (g - s * SH::GPW);
-        float part[V];
-#pragma unroll
-        for (int i = 0; i < V; i++) part[i] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kRows; j++) {
-            if (r0 + j >= N) continue;  // warp-uniform
-            uint32_t sc = 0;
-            if (active) {
-                const int pp = problem_of(P, r0 + j);
-                const uint32_t lr = static_cast<uint32_t>(r0 + j - P.row0[pp]);
-                const int off = static_cast<int>(((lr * static_cast<uint32_t>(G) + s * SH::GPW) * 2u) & 15u) + goff;
-                sc = *reinterpret_cast<const uint16_t*>(st + SH::STAGE_CODES + j * SH::SWIN + off);
+        for (int64_t t = 0; t < my_blocks; t++) {
+            const int st = static_cast<int>(t % L.ST);
+            const int par = static_cast<int>(t / L.ST) & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, deadline))) {
+                record_error(12);
+                break;
             }
-            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
-            const uint32_t m = (sb >> 13) & 0x3FFu;
-            const float pow2 = __uint_as_float(sb & 0xFF800000u);  // +-2^E, or 0 for a zero scale
-            const uint4 tl = vtab[m + (m & ~7u)];
-            const uint4 th = vtab[m + (m & ~7u) + 8];
-            float a0[MT], a1[MT];
+            const uint8_t* stg = ring + st * L.stage_bytes;
+            float part[V];
 #pragma unroll
-            for (int tt = 0; tt < MT; tt++) a0[tt] = a1[tt] = 0.0f;
+            for (int i = 0; i < V; i++) part[i] = 0.0f;
+            // Row prologues first (metadata -> scale -> table is a chain of dependent shared-memory
+            // loads), for all of this warp's rows of the block, so that their latencies overlap.
+            uint4 tl[RMAX], th[RMAX];
+            float pow2[RMAX];
+            bool rv[RMAX];
 #pragma unroll
-            for (int c = 0; c < SH::CHUNKS; c++) {
-                const uint4 cw = lds128(st + ((j * 32 + lane) * SH::CHUNKS + (c ^ sw)) * 16);
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            for (int jj = 0; jj < RMAX; jj++) {
+                const int j = q * L.R + jj;
+                const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * j);
+                rv[jj] = jj < L.R && meta.valid && meta.problem < P.count;  // warp-uniform
+                uint32_t sc = 0;
+                if (rv[jj] && active)
+                    sc = *reinterpret_cast<const uint16_t*>(stg + L.scales_off + j * L.swin + meta.scale_off + 2 * g);
+                const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
+                const uint32_t m = (sb >> 13) & 0x3FFu;
+                pow2[jj] = __uint_as_float(sb & 0xFF800000u);  // +-2^E, or 0 for a zero scale
+                tl[jj] = vtab[m + (m & ~7u)];
+                th[jj] = vtab[m + (m & ~7u) + 8];
+            }
 #pragma unroll
-                for (int wi = 0; wi < 4; wi++) {
-                    uint32_t wp[4];
-                    lookup8(words[wi], tl, th, m1, p16, wp);
+            for (int jj = 0; jj < RMAX; jj++) {
+                if (!rv[jj]) continue;  // warp-uniform
+                const int j = q * L.R + jj;
+                float a0[MT], a1[MT];
 #pragma unroll
-                    for (int tt = 0; tt < MT; tt++) {
+                for (int tt = 0; tt < MT; tt++) a0[tt] = a1[tt] = 0.0f;
+                const uint8_t* crow = stg + j * L.row_code_bytes + s * 32 * CB + lane * CB;
 #pragma unroll
-                        for (int p = 0; p < 4; p++)
-                            fma_bf16x2(a0[tt], a1[tt], wp[p], xr[tt][4 * (4 * c + wi) + p]);
+                for (int c = 0; c < CHUNKS; c++) {
+                    const uint4 cw = lds128(crow + 16 * (c ^ sw));
+                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; wi++) {
+                        uint32_t wp[4];
+                        lookup8(words[wi], tl[jj], th[jj], m1, p16, wp);
+#pragma unroll
+                        for (int tt = 0; tt < MT; tt++) {
+#pragma unroll
+                            for (int p = 0; p < 4; p++)
+                                fma_bf16x2(a0[tt], a1[tt], wp[p], xr[tt][4 * (4 * c + wi) + p]);
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int tt = 0; tt < MT; tt++) part[j * MT + tt] = (a0[tt] + a1[tt]) * pow2;
-        }
-        __syncwarp();  // every lane is done with this stage before it is refilled
-        const float total = reduce_transposed<V>(part, lane);
-        constexpr int lanes_per_value = 32 / V;
-        const int idx = lane / lanes_per_value;
-        const bool writer = (lane % lanes_per_value) == 0 && idx < kRows * MT;
-        const int j = idx / MT, tt = idx % MT;
-        if (S == 1) {
-            if (writer && r0 + j < N) {
-                const int pp = problem_of(P, r0 + j);
-                const int np = P.row0[pp + 1] - P.row0[pp];
-                P.y[pp][static_cast<int64_t>(tt) * np + (r0 + j - P.row0[pp])] = bf16_bits(total);
+                for (int tt = 0; tt < MT; tt++) part[jj * MT + tt] = (a0[tt] + a1[tt]) * pow2[jj];
             }
-        } else {
-            const int64_t rb = blockIdx.x + t * gridDim.x;
-            float* buf = red + (t & 1) * S * rows_per_block * MT;
-            if (writer) buf[(s * rows_per_block + q * kRows + j) * MT + tt] = total;
-            __syncthreads();
-            for (int i = threadIdx.x; i < rows_per_block * MT; i += blockDim.x) {
-                const int64_t r = rb * rows_per_block + i / MT;
-                float acc = 0.0f;
-                for (int ss = 0; ss < S; ss++) acc += buf[ss * rows_per_block * MT + i];
-                if (r < N) {
-                    const int pp = problem_of(P, r);
-                    const int np = P.row0[pp + 1] - P.row0[pp];
-                    P.y[pp][static_cast<int64_t>(i % MT) * np + (r - P.row0[pp])] = bf16_bits(acc);
+            const float total = reduce_transposed<V>(part, lane);
+            constexpr int lanes_per_value = 32 / V;
+            const int idx = lane / lanes_per_value;
+            const bool writer = (lane % lanes_per_value) == 0 && idx < L.R * MT;
+            const int jj = idx / MT, tt = idx % MT;
+            if (L.S == 1) {
+                if (writer) {
+                    const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * (q * L.R + jj));
+                    if (meta.valid && meta.problem < P.count) {
+                        const int np = P.row0[meta.problem + 1] - P.row0[meta.problem];
+                        P.y[meta.problem][static_cast<int64_t>(tt) * np + meta.local_row] = bf16_bits(total);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + 8 * (L.ST + st));
+            } else {
+                float* red = reinterpret_cast<float*>(ring + st * L.stage_bytes + L.red_off);
+                if (writer) red[(s * L.RB + q * L.R + jj) * MT + tt] = total;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + 8 * (2 * L.ST + st));
+                if (warp == 0) {  // add the slices in order and release the stage
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, deadline))) {
+                        record_error(13);
+                        break;
+                    }
+                    for (int i = lane; i < L.RB * MT; i += 32) {
+                        const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * (i / MT));
+                        float acc = 0.0f;
+                        for (int ss = 0; ss < L.S; ss++) acc += red[ss * L.RB * MT + i];
+                        if (meta.valid && meta.problem < P.count) {
+                            const int np = P.row0[meta.problem + 1] - P.row0[meta.problem];
+                            P.y[meta.problem][static_cast<int64_t>(i % MT) * np + meta.local_row] = bf16_bits(acc);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars + 8 * (L.ST + st));
                 }
             }
         }
     }
-    cp_async_wait<0>();
 }
 
 struct TableState {
@@ -340,39 +383,46 @@ struct TableState {
 };
 TableState g_tables;
 
-template <int MT, int LPG, int R, int ST>
+template <int MT, int LPG>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
+    constexpr int CB = kGroup / LPG / 2;
+    constexpr int GPW = 32 / LPG;
     const int64_t N = P.row0[P.count];
-    using SH = GemvShape<MT, LPG, R, ST>;
-    constexpr int kRows = R;
     const int G = static_cast<int>(K / kGroup);
-    const int S = (G + SH::GPW - 1) / SH::GPW;
-    // Row lanes per slice: enough CTAs to cover the SMs when N is small, at most kMaxWarps warps.
-    const int64_t quads = (N + kRows - 1) / kRows;
-    int Q = static_cast<int>((quads + num_sms - 1) / num_sms);
-    const int qmax = S >= kMaxWarps ? 1 : kMaxWarps / S;
-    if (Q > qmax) Q = qmax;
-    if (Q < 1) Q = 1;
-    const int warps = S * Q;
-    const int rows_per_block = Q * kRows;
-    const int64_t blocks_needed = (N + rows_per_block - 1) / rows_per_block;
+    GemvLayout L = {};
+    L.S = (G + GPW - 1) / GPW;
+    // Rows per consumer warp: 2 for large matrices, 1 when that leaves SMs idle.
+    L.R = (N >= static_cast<int64_t>(2) * kMaxWarps * num_sms) ? 2 : 1;
+    int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
+    const int qmax = L.S >= kMaxWarps ? 1 : kMaxWarps / L.S;
+    L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
+    L.RB = L.Q * L.R;
+    L.row_code_bytes = static_cast<int>(K / 2);
+    L.swin = ((2 * G + 15) / 16 + 1) * 16;
+    L.scales_off = L.RB * L.row_code_bytes;
+    L.meta_off = L.scales_off + L.RB * L.swin;
+    L.red_off = L.meta_off + 16 * L.RB;
+    L.stage_bytes = L.red_off + ((L.S * L.RB * MT * 4 + 15) / 16) * 16;
+    // ring depth: as many stages as fit next to the V table (at most 8, at least 2)
+    const int budget = 227 * 1024 - kVtabBytes - 3 * 8 * 8 - 64;
+    L.ST = budget / L.stage_bytes;
+    if (L.ST > 8) L.ST = 8;
+    if (L.ST < 2) return cudaErrorInvalidValue;  // a row block does not fit twice
+    const int64_t blocks_needed = (N + L.RB - 1) / L.RB;
     const int grid = static_cast<int>(blocks_needed < num_sms ? blocks_needed : num_sms);
-    const size_t smem = kVtabBytes + static_cast<size_t>(warps) * SH::WARP_SMEM +
-                        (S > 1 ? 2 * static_cast<size_t>(S) * rows_per_block * MT * sizeof(float) : 0);
-    static std::once_flag attr_once[64];  // the largest request, set once per device
+    const size_t smem = kVtabBytes + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
+    static std::once_flag attr_once[64];  // the largest possible request, set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        const size_t max_smem = kVtabBytes + static_cast<size_t>(kMaxWarps) * SH::WARP_SMEM +
-                                2 * static_cast<size_t>(kMaxWarps) * kRows * MT * sizeof(float);
-        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG, R, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(max_smem));
+        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(32 * warps);
+    cfg.blockDim = dim3(32 * (L.S * L.Q + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -380,8 +430,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, R, ST>, x, P, static_cast<int>(K), S, Q, 0xFFFFFFFFu,
-                              0x10000u);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, P, static_cast<int>(K), L, 0xFFFFFFFFu, 0x10000u);
 }
 
 }  // namespace
@@ -516,19 +565,11 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
     if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
     P.row0[count] = static_cast<int>(rows);
     for (int i = count + 1; i <= kMaxGroup; i++) P.row0[i] = P.row0[count];
-    // HBM latency under load is a few microseconds, so each SM needs on the order of 100 KB of
-    // copies in flight: large matrices use 2 rows per warp iteration and a 5-deep ring (4 batches
-    // in flight per warp), smaller ones 1 row and an 8-deep ring so that many warps share the rows.
-    const bool large = rows >= static_cast<int64_t>(2) * kMaxWarps * num_sms;
     switch (M) {
-        case 1: return large ? launch_gemv_t<1, 1, 2, 5>(x, P, K, num_sms, stream)
-                             : launch_gemv_t<1, 1, 1, 8>(x, P, K, num_sms, stream);
-        case 2: return large ? launch_gemv_t<2, 2, 4, 2>(x, P, K, num_sms, stream)
-                             : launch_gemv_t<2, 2, 1, 4>(x, P, K, num_sms, stream);
-        case 3: return large ? launch_gemv_t<3, 2, 4, 2>(x, P, K, num_sms, stream)
-                             : launch_gemv_t<3, 2, 1, 4>(x, P, K, num_sms, stream);
-        case 4: return large ? launch_gemv_t<4, 2, 4, 2>(x, P, K, num_sms, stream)
-                             : launch_gemv_t<4, 2, 1, 4>(x, P, K, num_sms, stream);
+        case 1: return launch_gemv_t<1, 1>(x, P, K, num_sms, stream);
+        case 2: return launch_gemv_t<2, 2>(x, P, K, num_sms, stream);
+        case 3: return launch_gemv_t<3, 2>(x, P, K, num_sms, stream);
+        case 4: return launch_gemv_t<4, 2>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -23,8 +23,6 @@
 
 namespace nf4 {
 
-__device__ int g_tc_error;  // 0, or the code of the first bounded wait that timed out
-
 namespace tc {
 
 constexpr int kTileN = 128;   // weight rows per CTA (MMA M)
@@ -33,7 +31,6 @@ constexpr int kDequantWarps = 8;
 constexpr int kThreads = 32 * (2 + kDequantWarps);
 constexpr uint32_t kABytes = kTileN * 64 * 2;    // 16 KB
 constexpr uint32_t kCodeBytes = kTileN * 64 / 2;  // 4 KB
-constexpr long long kWaitCycles = 2000000000LL;    // ~1 s at 2 GHz
 constexpr long long kDrainCycles = 200000000LL;    // ~0.1 s
 
 template <int T>
@@ -45,36 +42,6 @@ struct Layout {
     static constexpr uint32_t kBytes = kBars + 256;
     static constexpr uint32_t kCols = T <= 32 ? 32 : (T <= 64 ? 64 : (T <= 128 ? 128 : 256));
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait on phase `parity`; false once `deadline` (clock64) has passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long deadline) {
-    while (!mbar_test(bar, parity)) {
-        if (clock64() > deadline) return false;
-    }
-    return true;
-}
-__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_tc_error, 0, code); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
