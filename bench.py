@@ -305,6 +305,23 @@ def run_reference(args, rank, world):
     }
 
 
+def profile_linear(m: int, n: int, k: int) -> None:
+    """Quantize one random n x k linear on the device and run nf4_linear four times (M = m), for
+    profiler captures of a single kernel; prints nothing to time."""
+    import nf4_weight_only_gb300 as nf4
+    from nf4_weight_only_gb300 import build, synth
+    build.build()
+    nf4.load()
+    dev = torch.device("cuda", 0)
+    codes, scales = nf4.quantize(synth.device_weights(1, n, k, dev))
+    x = synth.device_activations_bf16(2, m, k, dev)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    for _ in range(4):
+        nf4.nf4_linear(x, codes, scales, y)
+    torch.cuda.synchronize()
+    print(f"profile-linear M={m} N={n} K={k}: ok, device error word {nf4.nf4_check_device_error()}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -313,7 +330,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-linear", nargs=3, type=int, metavar=("M", "N", "K"),
+                    help="run one M x N x K linear four times (for single-kernel profiler captures) and exit")
     args = ap.parse_args()
+    if args.profile_linear:
+        profile_linear(*args.profile_linear)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":  # the oracle on host cores: rank 0 alone, no process group
