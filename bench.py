@@ -35,6 +35,18 @@ METRIC = "NF4 GEMV HBM GB/s (M=1) & % of peak; prefill TFLOP/s at M=32/512"
 LAYER_STEPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
 
+def decode_traffic_per_launch():
+    """DRAM bytes per decode launch from the committed ncu launch-list summary (None if absent)."""
+    import re
+    path = os.path.join(ROOT, "profiles", "gemv_decode_3b_launch_list.md")
+    try:
+        with open(path) as fh:
+            m = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", fh.read(), re.M)
+        return int(m.group(1)) if m else None
+    except OSError:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -206,7 +218,8 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (1.47 GB of packed weights per step)",
                    "graph": "one CUDA graph per step", "peak_source": pk["source"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": decode_traffic_per_launch(),
+                     "algorithmic_bytes_per_launch": int(algo / launches),
                      "kernel": "gemv_kernel<1,1>",
                      "note": "algorithmic bytes (codes+scales+x+y) per launch / average launch time over the "
                              "timed steps, inter-launch gaps included; peak of measured"},
