@@ -80,8 +80,11 @@ nf4_status nf4_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, 
 /*
  * nf4_linear - y = x * w_hat^T with the weights streamed in packed form and dequantized tile by
  * tile on chip (deep-fold README, execution-path table: N=1 decode GEMV, prefill GEMM of up to 32
- * positions; larger M is this library's extension).  M = 1 runs a CUDA-core GEMV, small M a
- * CUDA-core kernel, large M a tcgen05 tensor-core GEMM; the choice depends on M only.
+ * positions; larger M is this library's extension).  M <= 4 runs a CUDA-core GEMV (K up to 32768
+ * for M = 1, 16384 for M = 2..4); M <= 32, and M <= 4 with a longer K, run a weight-streaming
+ * kernel that dequantizes on the CUDA cores into tensor memory and multiplies on the tcgen05 tensor
+ * cores (one CTA per SM, K split into slices when a CTA has few rows); larger M runs a tcgen05 GEMM
+ * over 128-row weight tiles.  The kernel depends on M and K; the K split on M, N and the SM count.
  *   x       in   bf16 bits [M][K]
  *   codes   in   uint8 [N][K/2]
  *   scales  in   fp16 bits [N][K/64]
@@ -93,9 +96,10 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
 /*
  * nf4_linear_grouped - several linears that read the same x, y_i = x * w_hat_i^T for i < count
  * (for instance the q, k and v projections, or the gate and up projections, of one decoder layer;
- * the deep-fold README's execution-path table runs decode as GEMVs over such linears).  For M <= 4
- * the linears run as one CUDA-core launch over their concatenated rows; for larger M they run one
- * tensor-core GEMM after another on `stream`.  Results equal those of count nf4_linear calls.
+ * the deep-fold README's execution-path table runs decode as GEMVs over such linears).  For M <= 32
+ * the linears share one launch over their rows; for larger M they run one GEMM after another on
+ * `stream`.  Each y_i meets the nf4_linear bound and repeated calls give the
+ * same bytes; the K split can differ from a separate nf4_linear call, so low-order bits may too.
  *   x        in   bf16 bits [M][K], shared by all linears
  *   count    1 .. 8
  *   codes    host array of count device pointers; codes[i]: uint8 [Ns[i]][K/2]

@@ -115,11 +115,10 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
             if (j != i && overlap(ys[i], yb, ys[j], M * Ns[j] * 2)) return NF4_ERR_ALIAS;
         }
     }
-    if (M < nf4::kTcMinTokens && K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
     if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
-    if (M < nf4::kTcMinTokens) {
+    if (M <= nf4::kStreamMaxTokens) {
         // drop empty problems, keep the order
         const uint8_t* c[nf4::kMaxGroupedLinears];
         const uint16_t* sc[nf4::kMaxGroupedLinears];
@@ -134,7 +133,9 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
                 nn[k] = Ns[i];
                 k++;
             }
-        return from_cuda(nf4::launch_gemv_grouped(x, k, c, sc, yy, nn, M, K, sms, stream));
+        if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
+            return from_cuda(nf4::launch_gemv_grouped(x, k, c, sc, yy, nn, M, K, sms, stream));
+        return from_cuda(nf4::launch_stream(x, k, c, sc, yy, nn, M, K, sms, stream));
     }
     for (int i = 0; i < count; i++) {
         if (Ns[i] == 0) continue;
@@ -194,12 +195,13 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y)) return NF4_ERR_ALIGN;
     const int64_t yb = M * N * 2, xb = M * K * 2, cb = N * K / 2, sb = N * (K / NF4_GROUP_SIZE) * 2;
     if (overlap(y, yb, x, xb) || overlap(y, yb, codes, cb) || overlap(y, yb, scales, sb)) return NF4_ERR_ALIAS;
-    if (M < nf4::kTcMinTokens && K > nf4::gemv_max_k(M == 1 ? 1 : 2)) return NF4_ERR_SHAPE;
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
     if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
     if (M >= nf4::kTcMinTokens) return from_cuda(nf4::launch_tc(x, codes, scales, y, M, N, K, stream));
-    return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
+    if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
+        return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
+    return from_cuda(nf4::launch_stream(x, 1, &codes, &scales, &y, &N, M, K, sms, stream));
 }
 
 }  // extern "C"

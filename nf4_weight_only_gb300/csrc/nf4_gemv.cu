@@ -437,6 +437,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
 }  // namespace nf4
 
 #include "nf4_tc.cuh"
+#include "nf4_stream.cuh"
 
 namespace nf4 {
 namespace {
@@ -518,6 +519,142 @@ cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     if (M <= 64) return launch_tc_t<64>(x, codes, scales, y, M, N, K, stream);
     if (M <= 128) return launch_tc_t<128>(x, codes, scales, y, M, N, K, stream);
     return launch_tc_t<256>(x, codes, scales, y, M, N, K, stream);
+}
+
+namespace {
+
+// Small-M weight streaming on the tensor cores (nf4_stream.cuh): one CTA per SM, each with a balanced
+// range of rows of one problem.
+template <int T>
+cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t K, cudaStream_t stream) {
+    using C = st::Cfg<T>;
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    // x: bf16 [M][K] viewed as [M][G][64]; a box is T tokens x S consecutive groups x 64, which lands
+    // as pseudo-token rows t * S + s of 128 bytes (128-byte swizzle).  Groups past G and tokens past M
+    // read as zero.
+    CUtensorMap maps[2];
+    const int slices[2] = {1, P.s_rem};
+    for (int v = 0; v < 2; v++) {
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K) * 2};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(slices[v]), static_cast<cuuint32_t>(T)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&maps[v], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // codes of each linear: uint8 [N][K/2]; full tiles load 128 rows x 128 bytes (4 groups) with the
+    // 128-byte swizzle, partial tiles r_rem rows x 32 * load_span(s_rem) * s_rem bytes
+    st::CodeMaps cm = {};
+    const uint32_t rem_bytes = 32u * st::load_span(P.s_rem) * P.s_rem;
+    for (int i = 0; i < P.count; i++) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(P.n[i])};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t estr[2] = {1, 1};
+        const cuuint32_t box_full[2] = {128, 128};
+        const cuuint32_t box_rem[2] = {rem_bytes, static_cast<cuuint32_t>(P.r_rem > 0 ? P.r_rem : 1)};
+        if (encode(&cm.full[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(P.codes[i]), dims, strides,
+                   box_full, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            encode(&cm.rem[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(P.codes[i]), dims, strides,
+                   box_rem, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   rem_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = C::kBytes + 1024;  // + slack to align the base to 1024 bytes
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(st::stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(P.cta0[P.count]));
+    cfg.blockDim = dim3(st::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, st::stream_kernel<T>, maps[0], maps[1], cm, P);
+}
+
+}  // namespace
+
+cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* codes, const uint16_t* const* scales,
+                          uint16_t* const* ys, const int64_t* Ns, int64_t M, int64_t K, int num_sms,
+                          cudaStream_t stream) {
+    if (count < 1 || count > st::kMaxProblems || M < 1 || M > kStreamMaxTokens || num_sms < 1)
+        return cudaErrorInvalidValue;
+    const int64_t G = K / kGroup;
+    int64_t total = 0;
+    for (int i = 0; i < count; i++) total += Ns[i];
+    if (total < 1) return cudaErrorInvalidValue;
+    // Rows per CTA: the smallest count that needs at most one CTA per SM (each CTA stays in one problem).
+    auto ctas = [&](int64_t r) {
+        int64_t c = 0;
+        for (int i = 0; i < count; i++) c += (Ns[i] + r - 1) / r;
+        return c;
+    };
+    int64_t rpc = (total + num_sms - 1) / num_sms;
+    if (rpc < 1) rpc = 1;
+    while (ctas(rpc) > num_sms) rpc++;
+    st::Params P = {};
+    P.count = count;
+    int64_t c = 0;
+    for (int i = 0; i < count; i++) {
+        P.codes[i] = codes[i];
+        P.scales[i] = scales[i];
+        P.y[i] = ys[i];
+        P.n[i] = static_cast<int>(Ns[i]);
+        P.cta0[i] = static_cast<int>(c);
+        c += (Ns[i] + rpc - 1) / rpc;
+    }
+    for (int i = count; i <= st::kMaxProblems; i++) P.cta0[i] = static_cast<int>(c);
+    P.rstar = static_cast<int>(rpc);
+    P.M = static_cast<int>(M);
+    P.K = static_cast<int>(K);
+    P.G = static_cast<int>(G);
+    P.m1 = 0xFFFFFFFFu;
+    P.p16 = 0x10000u;
+    // K-slices of a partial tile: as many as fit 128 MMA rows, the B tile's pseudo-token columns and G.
+    P.r_rem = static_cast<int>(rpc % 128);
+    auto slices = [&](int smax) {
+        int64_t s = P.r_rem ? 128 / P.r_rem : 1;
+        if (s > smax) s = smax;
+        if (s > G) s = G;
+        return static_cast<int>(s < 1 ? 1 : s);
+    };
+    if (M == 1) {
+        P.s_rem = slices(st::Cfg<1>::kSMax);
+        return launch_stream_t<1>(x, P, M, K, stream);
+    }
+    if (M == 2) {
+        P.s_rem = slices(st::Cfg<2>::kSMax);
+        return launch_stream_t<2>(x, P, M, K, stream);
+    }
+    if (M <= 4) {
+        P.s_rem = slices(st::Cfg<4>::kSMax);
+        return launch_stream_t<4>(x, P, M, K, stream);
+    }
+    if (M <= 8) {
+        P.s_rem = slices(st::Cfg<8>::kSMax);
+        return launch_stream_t<8>(x, P, M, K, stream);
+    }
+    if (M <= 16) {
+        P.s_rem = slices(st::Cfg<16>::kSMax);
+        return launch_stream_t<16>(x, P, M, K, stream);
+    }
+    P.s_rem = slices(st::Cfg<32>::kSMax);
+    return launch_stream_t<32>(x, P, M, K, stream);
 }
 
 cudaError_t read_and_clear_error(int* code) {

@@ -1,0 +1,587 @@
+// NF4 weight streaming for small M (decode and prefill up to 32 positions) on the tcgen05 tensor
+// cores, sm_103a.
+//
+// y[M, N] = x[M, K] * w_hat[N, K]^T for 1 <= M <= 32 (deep-fold README, execution-path table: the
+// N=1 decode GEMV and the prefill GEMM of up to 32 positions, both dequantizing only the current
+// tile of the packed weights).  These shapes are bound by the weight stream and by the integer work
+// of the 16-entry lookups, not by multiply-add throughput, so this kernel moves every multiply-add
+// onto the tensor cores and leaves the CUDA cores the lookups alone:
+//
+//   dequant warps:  packed codes (shared memory) -> exact bf16 w_hat -> tensor memory (tcgen05.st)
+//   one thread:     tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
+//                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
+//
+// K-slices.  A CTA owns a contiguous range of output rows, processed as tiles of R rows.  The 128
+// MMA rows of a tile are R rows x S K-slices (R * S <= 128): MMA row i = r * S + s holds row r's
+// groups s, S + s, 2S + s, ...; stage kb covers groups kb*S .. kb*S + S - 1, which are contiguous in
+// memory for every row.  The B tile holds, for each token t and slice s, the 64 x values of group
+// kb*S + s as pseudo-token column j = t * S + s, so D[r*S + s][t*S + s] is row r's partial sum over
+// slice s; the epilogue adds the S partials of each (row, token) in slice order.  The off-diagonal
+// columns are computed and dropped (the tensor cores have the throughput to spare).  This lets a
+// CTA with only a dozen rows still fill all 128 MMA rows and all 128 dequant lanes, so the grid is
+// one CTA per SM with a balanced row range each, for any N.
+//
+// Rings.  Codes move in load stages of U k-stages (one TMA box of all rows x U*S groups, 128 bytes a
+// row where possible: the TMA engine moves short rows slowly); x moves per k-stage (one box of T
+// tokens x S groups); scales per 8 k-stages (zero-filling 16-byte copies of each row's window).  The
+// codes ring is released by the dequant warps, the x ring by the MMAs, and the tensor-memory ring of
+// A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
+//
+// Warp roles (320 threads): warp 0 produces (lane 0 issues the TMA boxes, the warp copies scales),
+// warp 1 owns tensor memory and one lane issues the MMAs, warps 2-9 are two sets of four dequant
+// warps (a set takes every other k-stage; the four warps of a set cover the four 32-lane quarters of
+// tensor memory) that also run the epilogue of every other tile.  Weights do not depend on the
+// previous kernel in the stream, so codes and scales are requested before the programmatic-
+// dependent-launch wait; only x and y wait for it.  At M = 1 the kernel needs 256 tensor-memory
+// columns and ~110 KB of shared memory, so the next kernel's CTA can start on the same SM while this
+// one drains.
+//
+// The V table is the 1024-row half (32 KB) of the per-device table: an odd scale exponent is folded
+// in registers instead (flip the exponent's low bit in the low byte, carry into the high byte).
+// Every mbarrier wait is bounded; a wait that runs out records an error code, drains the copies and
+// MMAs in flight (bounded again) and frees tensor memory.
+#pragma once
+
+namespace nf4 {
+namespace st {
+
+constexpr int kSets = 2;                        // dequant warp sets
+constexpr int kThreads = 32 * (2 + 4 * kSets);  // 320
+constexpr uint32_t kScaleSlot = 6144;           // R * (S + 2) 16-byte chunks with R * S <= 128
+constexpr uint32_t kLoadBytes = 16384;          // one codes load stage: <= 128 MMA rows x 128 bytes
+constexpr int kMaxProblems = 8;
+constexpr long long kDrainCycles = 200000000LL;
+
+// Four accumulators: K-step ks of every stage goes to accumulator ks, so that no MMA waits for the
+// previous one to finish (with N of 16..64 an MMA is short); the epilogue adds the four in order.
+constexpr int kAcc = 4;
+
+template <int T>
+struct Cfg {
+    static constexpr int kTmemCols = T == 1 ? 256 : 512;            // 256: a second CTA fits on the SM
+    static constexpr int kJMax = T == 1 ? 16 : (T <= 4 ? 32 : 64);  // pseudo-token columns of B and of each D
+    static constexpr int kSMax = kJMax / T < 8 ? kJMax / T : 8;     // K-slices per tile
+    static constexpr int kDCols = kAcc * kJMax;                     // accumulators in tensor memory
+    static constexpr int kAStages = (kTmemCols - kDCols) / 32 < 8 ? (kTmemCols - kDCols) / 32 : 8;
+    static_assert(kAStages % 2 == 0, "a dequant set must own the same A slots in every round");
+    static constexpr int kXStages = 8;
+    static constexpr int kLoadStages = T == 1 ? 3 : 4;
+    static constexpr int kScaleStages = T == 1 ? 2 : 3;
+    static constexpr uint32_t kXBytes = kJMax * 128;  // multiple of 1024
+    static constexpr uint32_t kOffCodes = kXStages * kXBytes;
+    static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
+    static constexpr uint32_t kOffScales = kOffVtab + 32768;
+    static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
+    static constexpr uint32_t kOffBars = kOffRed + 128 * T * 4;
+    static constexpr uint32_t kBytes = kOffBars + 512;
+};
+
+// k-stages per codes load stage for a tile of S slices: 128 bytes a row for S = 1, 2, 4.
+__host__ __device__ constexpr int load_span(int s) { return s == 1 ? 4 : (s == 2 ? 2 : 1); }
+
+struct Params {
+    const uint8_t* codes[kMaxProblems];
+    const uint16_t* scales[kMaxProblems];
+    uint16_t* y[kMaxProblems];
+    int n[kMaxProblems];            // rows of each problem
+    int cta0[kMaxProblems + 1];     // first CTA of each problem; cta0[count] = grid size
+    int count;
+    int rstar;                      // rows per CTA (the last CTA of a problem may have fewer)
+    int r_rem;                      // rows of a CTA's partial tile (rstar % 128; 0 = none)
+    int s_rem;                      // its K-slices (r_rem * s_rem <= 128)
+    int M, K, G;
+    uint32_t m1, p16;               // 0xFFFFFFFF and 0x10000 (multipliers of the lookup, see lookup8)
+};
+
+// Codes of each problem, uint8 [N][K/2]: full tiles load boxes of 128 rows x 128 bytes (4 groups,
+// 128-byte swizzle), partial tiles r_rem rows x 32 * load_span(s_rem) * s_rem bytes (128-byte swizzle
+// when that is 128 bytes).  Rows past N and bytes past K/2 read as zero.
+struct CodeMaps {
+    CUtensorMap full[kMaxProblems];
+    CUtensorMap rem[kMaxProblems];
+};
+
+struct Tile {
+    int row0, rows, s, nt;  // first row (in the problem), rows, K-slices, k-stages
+};
+
+__device__ __forceinline__ Tile tile_of(const Params& P, int rbeg, int rows_cta, int j) {
+    const int nfull = rows_cta / 128;
+    Tile t;
+    if (j < nfull) {
+        t.row0 = rbeg + 128 * j;
+        t.rows = 128;
+        t.s = 1;
+    } else {
+        t.row0 = rbeg + 128 * nfull;
+        t.rows = rows_cta - 128 * nfull;
+        t.s = t.rows <= P.r_rem ? P.s_rem : 1;  // a partial tile that fits the partial box
+    }
+    t.nt = (P.G + t.s - 1) / t.s;
+    return t;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// D[128 x N] (+)= A[128 x 16] * B[N x 16]^T with A read from tensor memory.
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_n(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (8u << 24);
+}
+
+// Bounded wait by all 32 lanes (warp-uniform result).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long deadline) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, deadline));
+}
+
+// Bounded wait by lane 0 alone, result broadcast to the warp.
+__device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, long long deadline, int lane) {
+    bool w = true;
+    if (lane == 0) w = mbar_wait(bar, parity, deadline);
+    return __shfl_sync(0xFFFFFFFFu, w, 0);
+}
+
+template <int T>
+__global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
+    stream_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
+                  const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
+    using C = Cfg<T>;
+    constexpr int NA = C::kAStages, NX = C::kXStages, NL = C::kLoadStages, NSS = C::kScaleStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = P.G;
+
+    // barriers
+    const uint32_t b_lfull = sbase + C::kOffBars;       // [NL] codes load stage landed (tx)
+    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage read (8 dequant warps)
+    const uint32_t b_xfull = b_lempty + 8 * NL;         // [NX] x tile landed (tx)
+    const uint32_t b_xempty = b_xfull + 8 * NX;         // [NX] x tile read by the MMAs (commit)
+    const uint32_t b_afull = b_xempty + 8 * NX;         // [NA] A tile in tensor memory (4 warps)
+    const uint32_t b_aempty = b_afull + 8 * NA;         // [NA] A tile read by the MMAs (commit)
+    const uint32_t b_sfull = b_aempty + 8 * NA;         // [NSS] scale tile landed (32 producer lanes)
+    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile read (8 dequant warps)
+    // accumulators complete (commit), one barrier per epilogue set: a set waits only for its own
+    // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
+    const uint32_t b_dfull = b_sempty + 8 * NSS;        // [2]
+    const uint32_t b_dfree = b_dfull + 16;              // accumulators read (4 warps)
+    const uint32_t b_ep = b_dfree + 8;                  // [2] per-set epilogue rendezvous
+    const uint32_t b_mdone = b_ep + 16;                 // every MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + 6));
+
+    // this CTA's problem and rows
+    int p = 0;
+    for (int i = 1; i < P.count; i++)
+        if (static_cast<int>(blockIdx.x) >= P.cta0[i]) p = i;
+    const int rbeg = (static_cast<int>(blockIdx.x) - P.cta0[p]) * P.rstar;
+    const int rows_cta = P.n[p] - rbeg < P.rstar ? P.n[p] - rbeg : P.rstar;
+    const int ntiles = rows_cta / 128 + (rows_cta % 128 != 0);
+
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NL; i++) {
+            mbar_init(b_lfull + 8 * i, 1);
+            mbar_init(b_lempty + 8 * i, 4 * kSets);
+        }
+        for (int i = 0; i < NX; i++) {
+            mbar_init(b_xfull + 8 * i, 1);
+            mbar_init(b_xempty + 8 * i, 1);
+        }
+        for (int i = 0; i < NA; i++) {
+            mbar_init(b_afull + 8 * i, 4);
+            mbar_init(b_aempty + 8 * i, 1);
+        }
+        for (int i = 0; i < NSS; i++) {
+            mbar_init(b_sfull + 8 * i, 32);
+            mbar_init(b_sempty + 8 * i, 4 * kSets);
+        }
+        mbar_init(b_dfull, 1);
+        mbar_init(b_dfull + 8, 1);
+        mbar_init(b_dfree, 4);
+        mbar_init(b_ep, 4);
+        mbar_init(b_ep + 8, 4);
+        mbar_init(b_mdone, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < 2048; i += kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
+    cp_async_commit();
+    cp_async_wait<0>();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const long long deadline = clock64() + kWaitCycles;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        // Lane 0 issues the TMA boxes; the warp copies scale windows.  Ring positions are counters.
+        const uint8_t* sbytes = reinterpret_cast<const uint8_t*>(P.scales[p]);
+        const int64_t s_total = static_cast<int64_t>(P.n[p]) * G * 2;
+        const CUtensorMap* cm_full = &cmaps.full[p];
+        const CUtensorMap* cm_rem = &cmaps.rem[p];
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_full)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_rem)) : "memory");
+        }
+        bool ok = true, x_on = false;
+        int kq = 0, xslot = 0, xround = 0, lq = 0, lslot = 0, lround = 0, sslot = 0, sround = 0;
+        // x of the first `upto` k-stages (ring round 0), once the previous grid has finished
+        auto send_early_x = [&](int upto) {
+            pdl_wait();
+            int qq = 0;
+            for (int jj = 0; jj < ntiles && qq < upto; jj++) {
+                const Tile tt = tile_of(P, rbeg, rows_cta, jj);
+                const CUtensorMap* xm = tt.s > 1 ? &x_rem : &x_full;
+                for (int g = 0; g < G && qq < upto; g += tt.s, qq++) {
+                    mbar_expect_tx(b_xfull + 8 * qq, 128u * tt.s * T);
+                    tma_load_3d(sbase + qq * C::kXBytes, xm, 0, g, 0, b_xfull + 8 * qq);
+                }
+            }
+        };
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int U = load_span(t.s);
+            const CUtensorMap* cmap = t.s > 1 ? cm_rem : cm_full;
+            const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;
+            const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
+            const uint32_t xbytes = 128u * t.s * T;
+            const uint32_t per_row = (t.s + 2) * 16;
+            for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
+                if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
+                    if (lround > 0 && !lane0_wait(b_lempty + 8 * lslot, (lround - 1) & 1, deadline, lane)) {
+                        if (lane == 0) record_error(21);
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_expect_tx(b_lfull + 8 * lslot, cbytes);
+                        tc::tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes, cmap, g * 32, t.row0,
+                                        b_lfull + 8 * lslot);
+                    }
+                    lq++;
+                    if (++lslot == NL) {
+                        lslot = 0;
+                        lround++;
+                    }
+                }
+                if ((kb & 7) == 0) {  // scale tile: groups g .. g + 8S - 1 of every row
+                    if (sround > 0 && !warp_wait(b_sempty + 8 * sslot, (sround - 1) & 1, deadline)) {
+                        if (lane == 0) record_error(22);
+                        ok = false;
+                        break;
+                    }
+                    const int g1 = g + 8 * t.s < G ? g + 8 * t.s : G;
+                    uint8_t* dst = smem + C::kOffScales + sslot * kScaleSlot;
+                    for (int r = lane; r < t.rows; r += 32) {
+                        const int64_t rb = static_cast<int64_t>(t.row0 + r) * G * 2;
+                        const int64_t a = (rb + 2 * g) & ~static_cast<int64_t>(15);
+                        for (int64_t c = a; c < rb + 2 * g1; c += 16) {
+                            const int64_t left = s_total - c;
+                            cp_async16(dst + r * per_row + (c - a), sbytes + c, static_cast<uint32_t>(left < 16 ? left : 16));
+                        }
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_sfull + 8 * sslot)
+                                 : "memory");
+                    if (++sslot == NSS) {
+                        sslot = 0;
+                        sround++;
+                    }
+                }
+                if (xround > 0) {  // reusing an x slot: the MMAs of k-stage kq - NX have completed
+                    if (!x_on) {   // the x ring is full: wait for the previous grid, then send x
+                        if (lane == 0) send_early_x(NX);
+                        x_on = true;
+                    }
+                    if (!lane0_wait(b_xempty + 8 * xslot, (xround - 1) & 1, deadline, lane)) {
+                        if (lane == 0) record_error(23);
+                        ok = false;
+                        break;
+                    }
+                }
+                if (x_on && lane == 0) {
+                    mbar_expect_tx(b_xfull + 8 * xslot, xbytes);
+                    tma_load_3d(sbase + xslot * C::kXBytes, xmap, 0, g, 0, b_xfull + 8 * xslot);
+                }
+                __syncwarp();
+                kq++;
+                if (++xslot == NX) {
+                    xslot = 0;
+                    xround++;
+                }
+            }
+        }
+        if (ok && !x_on) {  // fewer k-stages than x slots
+            if (lane == 0) send_early_x(kq);
+            x_on = true;
+        }
+        cp_async_wait<0>();
+        // drain: the copies of the last ring rounds have landed before the CTA may exit
+        if (lane == 0) {
+            const long long dl = clock64() + kDrainCycles;
+            for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, dl);
+            for (int qq = kq - NX > 0 ? kq - NX : 0; qq < kq; qq++) mbar_wait(b_xfull + 8 * (qq % NX), (qq / NX) & 1, dl);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            int aslot = 0, xslot = 0;
+            uint32_t aph = 0, xph = 0;
+            for (int j = 0; j < ntiles && ok; j++) {
+                const Tile t = tile_of(P, rbeg, rows_cta, j);
+                const int nmma = (T * t.s + 15) & ~15;
+                const uint32_t idesc = idesc_n(nmma < 16 ? 16 : nmma);
+                if (j > 0 && !mbar_wait(b_dfree, (j - 1) & 1, deadline)) {
+                    record_error(24);
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                for (int kb = 0; kb < t.nt; kb++) {
+                    if (!mbar_wait(b_afull + 8 * aslot, aph, deadline) || !mbar_wait(b_xfull + 8 * xslot, xph, deadline)) {
+                        record_error(25);
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t a_tmem = tmem_base + C::kDCols + 32 * aslot;
+                    const uint64_t bdesc = tc::smem_desc_sw128(sbase + xslot * C::kXBytes);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ks++)  // K = 16 per MMA: 8 columns of A, 32 bytes of B
+                        mma_tmem_a(tmem_base + ks * C::kJMax, a_tmem + 8 * ks, bdesc + 2 * ks, idesc, kb != 0);
+                    tc::mma_commit(b_aempty + 8 * aslot);
+                    tc::mma_commit(b_xempty + 8 * xslot);
+                    if (++aslot == NA) {
+                        aslot = 0;
+                        aph ^= 1;
+                    }
+                    if (++xslot == NX) {
+                        xslot = 0;
+                        xph ^= 1;
+                    }
+                }
+                if (ok) tc::mma_commit(b_dfull + 8 * (j & (kSets - 1)));
+            }
+            tc::mma_commit(b_mdone);  // the CTA exits only after every MMA it issued has completed
+            mbar_wait(b_mdone, 0, clock64() + kDrainCycles);
+        }
+    } else {
+        // ---------------------------------------------------------------- dequant + epilogue
+        const int set = (warp - 2) >> 2;
+        const int quarter = warp & 3;             // tensor-memory lanes this warp may access
+        const int i = quarter * 32 + lane;        // MMA row
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint4* vtab = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
+        bool ok = true;
+        int q = 0, aslot = 0, around = 0, lslot = 0, sslot = 0, ep_uses = 0;
+        uint32_t lph = 0, sph = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int U = load_span(t.s);
+            const int r = i / t.s, sl = i - (i / t.s) * t.s;
+            const bool lane_ok = r < t.rows;
+            const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
+            // codes of row r in a load stage: rowb bytes, 16-byte chunks permuted by the 128-byte
+            // swizzle (chunk ^ (r mod 8)) when the row is 128 bytes
+            const uint32_t rowb = 32u * U * t.s;
+            const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
+            // this lane's scale inside a scale tile: row r's window starts at the 16-byte boundary
+            // below its first scale; stage kb adds 2 * (kb mod 8) * S bytes
+            const uint32_t soff = r * (t.s + 2) * 16 +
+                                  static_cast<uint32_t>((static_cast<int64_t>(t.row0 + r) * G * 2) & 15) + 2 * sl;
+            for (int kb = 0; kb < t.nt && ok; kb++) {
+                const int u = kb & (U - 1);
+                // every warp waits for every load stage and scale tile it passes, in order
+                if ((u == 0 && !warp_wait(b_lfull + 8 * lslot, lph, deadline)) ||
+                    ((kb & 7) == 0 && !warp_wait(b_sfull + 8 * sslot, sph, deadline))) {
+                    record_error(26);
+                    ok = false;
+                    break;
+                }
+                if ((q & (kSets - 1)) == set) {
+                    if (around > 0 && !warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline)) {
+                        record_error(27);
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    if (warp_ok) {
+                        uint32_t out[32];
+                        const int g = kb * t.s + sl;
+                        if (lane_ok && g < G) {
+                            const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + r * rowb;
+                            const uint32_t ch = static_cast<uint32_t>((u * t.s + sl) * 2);
+                            const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
+                            const uint16_t sc = *reinterpret_cast<const uint16_t*>(
+                                smem + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s);
+                            // scale = sign * 2^E * (1 + m/1024); w_hat = 2^E * V[m][c]: the table row
+                            // gives V, E is added to the exponent field of every entry.  An odd E flips
+                            // the exponent's low bit (bit 7 of the low byte) and carries into the high
+                            // byte; E >> 1 is added to the high byte (exponent >> 1), byte by byte.
+                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
+                            const uint32_t m = (sb >> 13) & 0x3FFu;
+                            const int e = static_cast<int>((sb >> 23) & 0xFFu) - 127;
+                            const uint32_t pm = (e & 1) ? 0x80808080u : 0u;
+                            const uint32_t add = static_cast<uint32_t>(e >> 1) * 0x01010101u;
+                            const uint32_t sgn = (sb >> 31) ? 0x80808080u : 0u;
+                            uint4 tl = vtab[m + (m & ~7u)];
+                            uint4 th = vtab[m + (m & ~7u) + 8];
+                            th.x = (th.x + add + ((tl.x & pm) >> 7)) ^ sgn;
+                            th.y = ((th.y + add + ((tl.y & pm) >> 7)) & 0x00FFFFFFu) ^ sgn;  // code 7 stays 0
+                            th.z = (th.z + add + ((tl.z & pm) >> 7)) ^ sgn;
+                            th.w = (th.w + add + ((tl.w & pm) >> 7)) ^ sgn;
+                            tl.x ^= pm;
+                            tl.y = (tl.y ^ pm) & 0x00FFFFFFu;
+                            tl.z ^= pm;
+                            tl.w ^= pm;
+                            if ((sb & 0x7FFFFFFFu) == 0u) {  // zero scale
+                                tl = make_uint4(0, 0, 0, 0);
+                                th = make_uint4(0, 0, 0, 0);
+                            }
+                            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                            for (int w = 0; w < 8; w++) {
+                                uint32_t o4[4];
+                                lookup8(words[w], tl, th, P.m1, P.p16, o4);
+                                out[4 * w + 0] = o4[0];
+                                out[4 * w + 1] = o4[1];
+                                out[4 * w + 2] = o4[2];
+                                out[4 * w + 3] = o4[3];
+                            }
+                        } else {
+#pragma unroll
+                            for (int w = 0; w < 32; w++) out[w] = 0u;
+                        }
+                        tmem_st32(tmem_base + lane_addr + C::kDCols + 32 * aslot, out);
+                    }
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_afull + 8 * aslot);
+                }
+                if (u == U - 1 || kb == t.nt - 1) {  // leaving a load stage
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_lempty + 8 * lslot);
+                    if (++lslot == NL) {
+                        lslot = 0;
+                        lph ^= 1;
+                    }
+                }
+                if ((kb & 7) == 7 || kb == t.nt - 1) {  // leaving a scale tile
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_sempty + 8 * sslot);
+                    if (++sslot == NSS) {
+                        sslot = 0;
+                        sph ^= 1;
+                    }
+                }
+                q++;
+                if (++aslot == NA) {
+                    aslot = 0;
+                    around++;
+                }
+            }
+            if (!ok || j % kSets != set) continue;
+            // ------------------------------------------------------------ epilogue of tile j
+            if (!warp_wait(b_dfull + 8 * set, (j / kSets) & 1, deadline)) {
+                record_error(26);
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            pdl_wait();  // y may still be read by the previous grid (returns at once by now)
+            const int M = P.M, np = P.n[p];
+            uint16_t* y = P.y[p];
+            float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+            const int J = T * t.s;
+            for (int c = 0; c < J; c += 16) {
+                uint32_t v[16];
+                tc::tmem_ld16(tmem_base + lane_addr + c, v);
+#pragma unroll
+                for (int a = 1; a < kAcc; a++) {  // add the accumulators in order
+                    uint32_t w[16];
+                    tc::tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++) v[cc] = __float_as_uint(__uint_as_float(v[cc]) + __uint_as_float(w[cc]));
+                }
+#pragma unroll
+                for (int cc = 0; cc < 16; cc++) {
+                    const int col = c + cc;
+                    if (t.s == 1) {
+                        if (lane_ok && col < M) y[static_cast<int64_t>(col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
+                    } else {
+                        const int rel = col - sl;
+                        const int tt = rel / t.s;
+                        if (rel >= 0 && rel == tt * t.s && tt < M) red[tt * 128 + i] = __uint_as_float(v[cc]);
+                    }
+                }
+            }
+            if (t.s > 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_ep + 8 * set);
+                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, deadline)) {
+                    record_error(27);
+                    ok = false;
+                    break;
+                }
+                ep_uses++;
+                for (int o = i; o < t.rows * M; o += 128) {
+                    const int tt = o / t.rows, rr = o - tt * t.rows;
+                    float acc = 0.0f;
+                    for (int s2 = 0; s2 < t.s; s2++) acc += red[tt * 128 + rr * t.s + s2];
+                    y[static_cast<int64_t>(tt) * np + t.row0 + rr] = bf16_bits(acc);
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dfree);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace st
+}  // namespace nf4

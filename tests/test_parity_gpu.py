@@ -310,10 +310,11 @@ def test_linear_negative_and_zero_scales(nf4, o):
 # ------------------------------------------------------------------------------------------------
 # grouped linears sharing x
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("m", [1, 3, 4, 7])
-def test_linear_grouped_matches_single(nf4, o, m):
-    """q, k and v of a 2048-wide layer (plus a ragged fourth) in one call equal separate calls and
-    meet the oracle bound."""
+@pytest.mark.parametrize("m", [1, 3, 4, 7, 32])
+def test_linear_grouped(nf4, o, m):
+    """q, k and v of a 2048-wide layer (plus a ragged fourth) in one call: every output meets the
+    oracle bound and a second call gives the same bytes.  (Separate calls may split K differently,
+    so their low-order bits are not required to match.)"""
     from nf4_weight_only_gb300 import synth
     k = 2048
     ns = [2048, 256, 256, 37]
@@ -326,13 +327,32 @@ def test_linear_grouped_matches_single(nf4, o, m):
         mats.append((c, s, torch.from_numpy(c).to(DEV),
                      torch.from_numpy(s.view(np.int16)).view(torch.float16).to(DEV)))
     ys = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for n in ns]
+    ys2 = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for n in ns]
     nf4.nf4_linear_grouped(xd, [t[2] for t in mats], [t[3] for t in mats], ys)
+    nf4.nf4_linear_grouped(xd, [t[2] for t in mats], [t[3] for t in mats], ys2)
     torch.cuda.synchronize()
-    for (c, s, cd, sd), y in zip(mats, ys):
-        single = torch.empty_like(y)
-        nf4.nf4_linear(xd, cd, sd, single)
-        torch.cuda.synchronize()
-        assert torch.equal(y.view(torch.int16), single.view(torch.int16))
+    assert device_error(nf4) == 0
+    for (c, s, cd, sd), y, y2 in zip(mats, ys, ys2):
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
         y64, mag = o.linear(x, c, s, nthreads=16)
         ok, ratio, _ = oracle.within_tolerance(dev_to_bits(y), y64, mag)
         assert ok, ratio
+
+
+# ------------------------------------------------------------------------------------------------
+# small-M tensor-core streaming (M <= 32): tiles of 128 rows plus a partial tile split into
+# K-slices, ragged last stages, every token-tile size
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("m", [5, 8, 16, 32])
+@pytest.mark.parametrize("n,k", [(2048, 11008), (22016, 2048), (19457, 640), (3, 27648)])
+def test_linear_stream_tiles(nf4, o, m, n, k):
+    check_linear(nf4, o, m, n, k, seed=7 * n + k + m)
+    assert device_error(nf4) == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 300, 36864), (1, 19457, 36864), (2, 150, 17408), (3, 2048, 20480),
+                                   (4, 129, 17408)])
+def test_linear_stream_long_k(nf4, o, m, n, k):
+    """M <= 4 with K past the GEMV's register-resident range runs the streaming kernel."""
+    check_linear(nf4, o, m, n, k, seed=11 * n + k + m)
+    assert device_error(nf4) == 0
