@@ -118,31 +118,23 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
     if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
-    if (M <= nf4::kStreamMaxTokens) {
-        // drop empty problems, keep the order
-        const uint8_t* c[nf4::kMaxGroupedLinears];
-        const uint16_t* sc[nf4::kMaxGroupedLinears];
-        uint16_t* yy[nf4::kMaxGroupedLinears];
-        int64_t nn[nf4::kMaxGroupedLinears];
-        int k = 0;
-        for (int i = 0; i < count; i++)
-            if (Ns[i] > 0) {
-                c[k] = codes[i];
-                sc[k] = scales[i];
-                yy[k] = ys[i];
-                nn[k] = Ns[i];
-                k++;
-            }
-        if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
-            return from_cuda(nf4::launch_gemv_grouped(x, k, c, sc, yy, nn, M, K, sms, stream));
-        return from_cuda(nf4::launch_stream(x, k, c, sc, yy, nn, M, K, sms, stream));
-    }
-    for (int i = 0; i < count; i++) {
-        if (Ns[i] == 0) continue;
-        if ((st = from_cuda(nf4::launch_tc(x, codes[i], scales[i], ys[i], M, Ns[i], K, stream))) != NF4_OK)
-            return st;
-    }
-    return NF4_OK;
+    // drop empty problems, keep the order
+    const uint8_t* c[nf4::kMaxGroupedLinears];
+    const uint16_t* sc[nf4::kMaxGroupedLinears];
+    uint16_t* yy[nf4::kMaxGroupedLinears];
+    int64_t nn[nf4::kMaxGroupedLinears];
+    int k = 0;
+    for (int i = 0; i < count; i++)
+        if (Ns[i] > 0) {
+            c[k] = codes[i];
+            sc[k] = scales[i];
+            yy[k] = ys[i];
+            nn[k] = Ns[i];
+            k++;
+        }
+    if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
+        return from_cuda(nf4::launch_gemv_grouped(x, k, c, sc, yy, nn, M, K, sms, stream));
+    return from_cuda(nf4::launch_stream(x, k, c, sc, yy, nn, M, K, sms, stream));
 }
 
 nf4_status nf4_check_device_error(int* code) {
@@ -198,7 +190,6 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
     if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
-    if (M >= nf4::kTcMinTokens) return from_cuda(nf4::launch_tc(x, codes, scales, y, M, N, K, stream));
     if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
         return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
     return from_cuda(nf4::launch_stream(x, 1, &codes, &scales, &y, &N, M, K, sms, stream));

@@ -436,7 +436,6 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
 }  // namespace
 }  // namespace nf4
 
-#include "nf4_tc.cuh"
 #include "nf4_stream.cuh"
 
 namespace nf4 {
@@ -458,68 +457,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-template <int T>
-cudaError_t launch_tc_t(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y, int64_t M,
-                        int64_t N, int64_t K, cudaStream_t stream) {
-    using L = tc::Layout<T>;
-    auto encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
-    CUtensorMap tx, tcodes;
-    {   // x: bf16 [M][K], boxes of 64 (K) x T (tokens), 128-byte swizzle; rows past M read as zero
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(T)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {   // codes: u8 [N][K/2], boxes of 32 bytes (one group) x 128 rows; rows past N read as zero
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(tc::kTileN)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    const size_t smem = L::kBytes + 1024;  // + slack to align the base to 1024 bytes
-    static std::once_flag attr_once[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(tc::gemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((N + tc::kTileN - 1) / tc::kTileN),
-                       static_cast<unsigned>((M + T - 1) / T));
-    cfg.blockDim = dim3(tc::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc::gemm_kernel<T>, tx, tcodes, scales, y, static_cast<int>(M),
-                              static_cast<int>(N), static_cast<int>(K), 0xFFFFFFFFu, 0x10000u);
-}
-
 }  // namespace
-
-cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y, int64_t M,
-                      int64_t N, int64_t K, cudaStream_t stream) {
-    if (M <= 16) return launch_tc_t<16>(x, codes, scales, y, M, N, K, stream);
-    if (M <= 32) return launch_tc_t<32>(x, codes, scales, y, M, N, K, stream);
-    if (M <= 64) return launch_tc_t<64>(x, codes, scales, y, M, N, K, stream);
-    if (M <= 128) return launch_tc_t<128>(x, codes, scales, y, M, N, K, stream);
-    return launch_tc_t<256>(x, codes, scales, y, M, N, K, stream);
-}
 
 namespace {
 
@@ -575,7 +513,7 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(P.cta0[P.count]));
+    cfg.gridDim = dim3(static_cast<unsigned>(P.cta0[P.count]), static_cast<unsigned>((M + T - 1) / T));
     cfg.blockDim = dim3(st::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -592,8 +530,32 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
 cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* codes, const uint16_t* const* scales,
                           uint16_t* const* ys, const int64_t* Ns, int64_t M, int64_t K, int num_sms,
                           cudaStream_t stream) {
-    if (count < 1 || count > st::kMaxProblems || M < 1 || M > kStreamMaxTokens || num_sms < 1)
-        return cudaErrorInvalidValue;
+    if (count < 1 || count > st::kMaxProblems || M < 1 || num_sms < 1) return cudaErrorInvalidValue;
+    if (M > 32) {  // wide tiles: one CTA per 128 rows x T tokens
+        st::Params P = {};
+        P.count = count;
+        int64_t c = 0;
+        for (int i = 0; i < count; i++) {
+            P.codes[i] = codes[i];
+            P.scales[i] = scales[i];
+            P.y[i] = ys[i];
+            P.n[i] = static_cast<int>(Ns[i]);
+            P.cta0[i] = static_cast<int>(c);
+            c += (Ns[i] + 127) / 128;
+        }
+        for (int i = count; i <= st::kMaxProblems; i++) P.cta0[i] = static_cast<int>(c);
+        P.rstar = 128;
+        P.r_rem = 0;
+        P.s_rem = 1;
+        P.M = static_cast<int>(M);
+        P.K = static_cast<int>(K);
+        P.G = static_cast<int>(K / kGroup);
+        P.m1 = 0xFFFFFFFFu;
+        P.p16 = 0x10000u;
+        if (M <= 64) return launch_stream_t<64>(x, P, M, K, stream);
+        if (M <= 128) return launch_stream_t<128>(x, P, M, K, stream);
+        return launch_stream_t<256>(x, P, M, K, stream);
+    }
     const int64_t G = K / kGroup;
     int64_t total = 0;
     for (int i = 0; i < count; i++) total += Ns[i];

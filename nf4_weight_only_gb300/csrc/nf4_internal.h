@@ -23,17 +23,11 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
                                 const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns, int64_t M,
                                 int64_t K, int num_sms, cudaStream_t stream);
 
-// Small-M weight streaming on the tensor cores (dequantized tiles in tensor memory): y_i[M, N_i] for
-// up to kMaxGroupedLinears linears that share x and K, 1 <= M <= kStreamMaxTokens, one launch.
-constexpr int kStreamMaxTokens = 32;
+// tcgen05 weight streaming (dequantized tiles in tensor memory) for every M the GEMV does not take:
+// y_i[M, N_i] for up to kMaxGroupedLinears linears that share x and K, one launch.
 cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* codes, const uint16_t* const* scales,
                           uint16_t* const* ys, const int64_t* Ns, int64_t M, int64_t K, int num_sms,
                           cudaStream_t stream);
-
-// tcgen05 tensor-core GEMM for M >= kTcMinTokens.
-constexpr int kTcMinTokens = kStreamMaxTokens + 1;
-cudaError_t launch_tc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
-                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 // Device error word of the tensor-core path (nonzero after a bounded pipeline wait timed out).
 cudaError_t read_and_clear_error(int* code);
 

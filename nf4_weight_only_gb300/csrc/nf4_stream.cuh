@@ -27,14 +27,12 @@
 // codes ring is released by the dequant warps, the x ring by the MMAs, and the tensor-memory ring of
 // A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
 //
-// Warp roles (320 threads): warp 0 produces (lane 0 issues the TMA boxes, the warp copies scales),
-// warp 1 owns tensor memory and one lane issues the MMAs, warps 2-9 are two sets of four dequant
-// warps (a set takes every other k-stage; the four warps of a set cover the four 32-lane quarters of
-// tensor memory) that also run the epilogue of every other tile.  Weights do not depend on the
-// previous kernel in the stream, so codes and scales are requested before the programmatic-
-// dependent-launch wait; only x and y wait for it.  At M = 1 the kernel needs 256 tensor-memory
-// columns and ~110 KB of shared memory, so the next kernel's CTA can start on the same SM while this
-// one drains.
+// Warp roles (352 threads): warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp
+// copies scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2-9 are two sets of
+// four dequant warps (a set takes every other stage; the four warps of a set cover the four 32-lane
+// quarters of tensor memory) that also run the epilogue of every other tile, warp 10 streams x.
+// Weights do not depend on the previous kernel in the stream, so warp 0 never waits for it; only x
+// and y do.  Each producer runs as far ahead as its own ring allows.
 //
 // The V table is the 1024-row half (32 KB) of the per-device table: an odd scale exponent is folded
 // in registers instead (flip the exponent's low bit in the low byte, carry into the high byte).
@@ -42,11 +40,14 @@
 // MMAs in flight (bounded again) and frees tensor memory.
 #pragma once
 
+#include <cuda.h>
+
 namespace nf4 {
 namespace st {
 
 constexpr int kSets = 2;                        // dequant warp sets
-constexpr int kThreads = 32 * (2 + 4 * kSets);  // 320
+constexpr int kXWarp = 2 + 4 * kSets;           // the x producer, after the dequant warps
+constexpr int kThreads = 32 * (kXWarp + 1);     // 352
 constexpr uint32_t kScaleSlot = 6144;           // R * (S + 2) 16-byte chunks with R * S <= 128
 constexpr uint32_t kLoadBytes = 16384;          // one codes load stage: <= 128 MMA rows x 128 bytes
 constexpr int kMaxProblems = 8;
@@ -56,23 +57,29 @@ constexpr long long kDrainCycles = 200000000LL;
 // previous one to finish (with N of 16..64 an MMA is short); the epilogue adds the four in order.
 constexpr int kAcc = 4;
 
+// T >= 64 ("wide"): a CTA owns one tile of 128 rows x T tokens, N = T per MMA (128 cycles at T = 256,
+// so one accumulator keeps the tensor pipe busy) and no K-slices.
 template <int T>
 struct Cfg {
-    static constexpr int kTmemCols = T == 1 ? 256 : 512;            // 256: a second CTA fits on the SM
-    static constexpr int kJMax = T == 1 ? 16 : (T <= 4 ? 32 : 64);  // pseudo-token columns of B and of each D
-    static constexpr int kSMax = kJMax / T < 8 ? kJMax / T : 8;     // K-slices per tile
-    static constexpr int kDCols = kAcc * kJMax;                     // accumulators in tensor memory
-    static constexpr int kAStages = (kTmemCols - kDCols) / 32 < 8 ? (kTmemCols - kDCols) / 32 : 8;
-    static_assert(kAStages % 2 == 0, "a dequant set must own the same A slots in every round");
-    static constexpr int kXStages = 8;
-    static constexpr int kLoadStages = T == 1 ? 3 : 4;
-    static constexpr int kScaleStages = T == 1 ? 2 : 3;
-    static constexpr uint32_t kXBytes = kJMax * 128;  // multiple of 1024
+    static constexpr bool kWide = T >= 64;
+    static constexpr int kAccN = kWide ? 1 : kAcc;                    // accumulators
+    static constexpr int kTmemCols = 512;
+    static constexpr int kJMax = kWide ? T : (T == 1 ? 16 : (T <= 4 ? 32 : 64));  // columns of B and of each D
+    static constexpr int kSMax = kWide ? 1 : (kJMax / T < 8 ? kJMax / T : 8);      // K-slices per tile
+    static constexpr int kDCols = kAccN * kJMax;                      // accumulators in tensor memory
+    // A slots of 64 columns (two groups of K per MMA row); an even count, so that each dequant set
+    // owns the same slots in every round
+    static constexpr int kAStages = ((kTmemCols - kDCols) / 64 < 8 ? (kTmemCols - kDCols) / 64 : 8) & ~1;
+    // ring depths (an x box of T rows takes ~1000-1500 cycles to arrive from L2)
+    static constexpr int kXStages = T <= 4 ? 12 : (T <= 64 ? 8 : (T == 128 ? 6 : 4));  // 64-k x sub-tiles
+    static constexpr int kLoadStages = T <= 128 ? (T == 128 ? 3 : 4) : 3;
+    static constexpr int kScaleStages = T == 256 ? 2 : 3;
+    static constexpr uint32_t kXBytes = kJMax * 128;  // one x sub-tile (multiple of 1024)
     static constexpr uint32_t kOffCodes = kXStages * kXBytes;
     static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
     static constexpr uint32_t kOffScales = kOffVtab + 32768;
     static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
-    static constexpr uint32_t kOffBars = kOffRed + 128 * T * 4;
+    static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
     static constexpr uint32_t kBytes = kOffBars + 512;
 };
 
@@ -102,7 +109,7 @@ struct CodeMaps {
 };
 
 struct Tile {
-    int row0, rows, s, nt;  // first row (in the problem), rows, K-slices, k-stages
+    int row0, rows, s, nt;  // first row (in the problem), rows, K-slices, 64-k sub-stages (even)
 };
 
 __device__ __forceinline__ Tile tile_of(const Params& P, int rbeg, int rows_cta, int j) {
@@ -117,8 +124,59 @@ __device__ __forceinline__ Tile tile_of(const Params& P, int rbeg, int rows_cta,
         t.rows = rows_cta - 128 * nfull;
         t.s = t.rows <= P.r_rem ? P.s_rem : 1;  // a partial tile that fits the partial box
     }
-    t.nt = (P.G + t.s - 1) / t.s;
+    t.nt = 2 * ((P.G + 2 * t.s - 1) / (2 * t.s));  // 64-k sub-stages, two per pipeline stage
     return t;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: next 8-row atom
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;                   // swizzle mode: 128 bytes
+    return d;
+}
+
+// Arrives on `bar` once every tcgen05.mma this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
@@ -171,7 +229,7 @@ __device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, long l
 }
 
 template <int T>
-__global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, 1)
     stream_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
                   const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
     using C = Cfg<T>;
@@ -206,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
     const int rbeg = (static_cast<int>(blockIdx.x) - P.cta0[p]) * P.rstar;
     const int rows_cta = P.n[p] - rbeg < P.rstar ? P.n[p] - rbeg : P.rstar;
     const int ntiles = rows_cta / 128 + (rows_cta % 128 != 0);
+    const int m0 = static_cast<int>(blockIdx.y) * T;  // first token of this CTA
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -232,8 +291,6 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
         mbar_init(b_ep + 8, 4);
         mbar_init(b_mdone, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -244,15 +301,17 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
     for (int i = threadIdx.x; i < 2048; i += kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
     cp_async_commit();
     cp_async_wait<0>();
-    tc::tc_fence_before();
+    tc_fence_before();
     __syncthreads();
-    tc::tc_fence_after();
+    tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const long long deadline = clock64() + kWaitCycles;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        // Lane 0 issues the TMA boxes; the warp copies scale windows.  Ring positions are counters.
+        // Codes and scales only (x has its own warp): weights do not depend on the previous grid, so
+        // this warp never waits for it and runs as far ahead as the codes ring allows.  Lane 0 issues
+        // the TMA boxes; the warp copies scale windows.  Ring positions are counters.
         const uint8_t* sbytes = reinterpret_cast<const uint8_t*>(P.scales[p]);
         const int64_t s_total = static_cast<int64_t>(P.n[p]) * G * 2;
         const CUtensorMap* cm_full = &cmaps.full[p];
@@ -261,28 +320,13 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_full)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_rem)) : "memory");
         }
-        bool ok = true, x_on = false;
-        int kq = 0, xslot = 0, xround = 0, lq = 0, lslot = 0, lround = 0, sslot = 0, sround = 0;
-        // x of the first `upto` k-stages (ring round 0), once the previous grid has finished
-        auto send_early_x = [&](int upto) {
-            pdl_wait();
-            int qq = 0;
-            for (int jj = 0; jj < ntiles && qq < upto; jj++) {
-                const Tile tt = tile_of(P, rbeg, rows_cta, jj);
-                const CUtensorMap* xm = tt.s > 1 ? &x_rem : &x_full;
-                for (int g = 0; g < G && qq < upto; g += tt.s, qq++) {
-                    mbar_expect_tx(b_xfull + 8 * qq, 128u * tt.s * T);
-                    tma_load_3d(sbase + qq * C::kXBytes, xm, 0, g, 0, b_xfull + 8 * qq);
-                }
-            }
-        };
+        bool ok = true;
+        int lq = 0, lslot = 0, lround = 0, sslot = 0, sround = 0;
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
             const int U = load_span(t.s);
             const CUtensorMap* cmap = t.s > 1 ? cm_rem : cm_full;
             const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;
-            const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
-            const uint32_t xbytes = 128u * t.s * T;
             const uint32_t per_row = (t.s + 2) * 16;
             for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
                 if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
@@ -293,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                     }
                     if (lane == 0) {
                         mbar_expect_tx(b_lfull + 8 * lslot, cbytes);
-                        tc::tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes, cmap, g * 32, t.row0,
-                                        b_lfull + 8 * lslot);
+                        tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes, cmap, g * 32, t.row0,
+                                    b_lfull + 8 * lslot);
                     }
                     lq++;
                     if (++lslot == NL) {
@@ -325,38 +369,44 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                         sround++;
                     }
                 }
-                if (xround > 0) {  // reusing an x slot: the MMAs of k-stage kq - NX have completed
-                    if (!x_on) {   // the x ring is full: wait for the previous grid, then send x
-                        if (lane == 0) send_early_x(NX);
-                        x_on = true;
-                    }
-                    if (!lane0_wait(b_xempty + 8 * xslot, (xround - 1) & 1, deadline, lane)) {
-                        if (lane == 0) record_error(23);
-                        ok = false;
-                        break;
-                    }
-                }
-                if (x_on && lane == 0) {
-                    mbar_expect_tx(b_xfull + 8 * xslot, xbytes);
-                    tma_load_3d(sbase + xslot * C::kXBytes, xmap, 0, g, 0, b_xfull + 8 * xslot);
-                }
                 __syncwarp();
-                kq++;
-                if (++xslot == NX) {
-                    xslot = 0;
-                    xround++;
-                }
             }
         }
-        if (ok && !x_on) {  // fewer k-stages than x slots
-            if (lane == 0) send_early_x(kq);
-            x_on = true;
-        }
         cp_async_wait<0>();
-        // drain: the copies of the last ring rounds have landed before the CTA may exit
+        // drain: the codes of the last ring round have landed before the CTA may exit
         if (lane == 0) {
             const long long dl = clock64() + kDrainCycles;
             for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, dl);
+        }
+    } else if (warp == kXWarp) {
+        // ---------------------------------------------------------------- x producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
+            pdl_wait();  // x may be written by the previous grid in the stream
+            bool ok = true;
+            int kq = 0, xslot = 0, xround = 0;
+            for (int j = 0; j < ntiles && ok; j++) {
+                const Tile t = tile_of(P, rbeg, rows_cta, j);
+                const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
+                const uint32_t xbytes = 128u * t.s * T;
+                for (int g = 0; g < t.nt * t.s; g += t.s) {  // a sub-stage: groups g .. g + S - 1
+                    if (xround > 0 && !mbar_wait(b_xempty + 8 * xslot, (xround - 1) & 1, deadline)) {
+                        record_error(23);
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(b_xfull + 8 * xslot, xbytes);
+                    tma_load_3d(sbase + xslot * C::kXBytes, xmap, 0, g, m0, b_xfull + 8 * xslot);
+                    kq++;
+                    if (++xslot == NX) {
+                        xslot = 0;
+                        xround++;
+                    }
+                }
+            }
+            // drain: the x tiles of the last ring round have landed before the CTA may exit
+            const long long dl = clock64() + kDrainCycles;
             for (int qq = kq - NX > 0 ? kq - NX : 0; qq < kq; qq++) mbar_wait(b_xfull + 8 * (qq % NX), (qq / NX) & 1, dl);
         }
     } else if (warp == 1) {
@@ -374,37 +424,48 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                     ok = false;
                     break;
                 }
-                tc::tc_fence_after();
-                for (int kb = 0; kb < t.nt; kb++) {
-                    if (!mbar_wait(b_afull + 8 * aslot, aph, deadline) || !mbar_wait(b_xfull + 8 * xslot, xph, deadline)) {
+                tc_fence_after();
+                for (int kb = 0; kb < t.nt / 2 && ok; kb++) {
+                    if (!mbar_wait(b_afull + 8 * aslot, aph, deadline)) {
                         record_error(25);
                         ok = false;
                         break;
                     }
-                    tc::tc_fence_after();
-                    const uint32_t a_tmem = tmem_base + C::kDCols + 32 * aslot;
-                    const uint64_t bdesc = tc::smem_desc_sw128(sbase + xslot * C::kXBytes);
+                    const uint32_t a_tmem = tmem_base + C::kDCols + 64 * aslot;
+                    for (int h = 0; h < 2; h++) {  // two 64-k sub-stages, each with its own x sub-tile
+                        if (!mbar_wait(b_xfull + 8 * xslot, xph, deadline)) {
+                            record_error(25);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t bdesc = smem_desc_sw128(sbase + xslot * C::kXBytes);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ks++)  // K = 16 per MMA: 8 columns of A, 32 bytes of B
-                        mma_tmem_a(tmem_base + ks * C::kJMax, a_tmem + 8 * ks, bdesc + 2 * ks, idesc, kb != 0);
-                    tc::mma_commit(b_aempty + 8 * aslot);
-                    tc::mma_commit(b_xempty + 8 * xslot);
+                        for (int ks = 0; ks < 4; ks++) {  // K = 16 per MMA: 8 columns of A, 32 bytes of B
+                            const int k8 = 4 * h + ks;
+                            mma_tmem_a(tmem_base + (k8 % C::kAccN) * C::kJMax, a_tmem + 8 * k8, bdesc + 2 * ks, idesc,
+                                       kb > 0 || k8 >= C::kAccN);
+                        }
+                        mma_commit(b_xempty + 8 * xslot);
+                        if (++xslot == NX) {
+                            xslot = 0;
+                            xph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(b_aempty + 8 * aslot);
                     if (++aslot == NA) {
                         aslot = 0;
                         aph ^= 1;
                     }
-                    if (++xslot == NX) {
-                        xslot = 0;
-                        xph ^= 1;
-                    }
                 }
-                if (ok) tc::mma_commit(b_dfull + 8 * (j & (kSets - 1)));
+                if (ok) mma_commit(b_dfull + 8 * (j & (kSets - 1)));
             }
-            tc::mma_commit(b_mdone);  // the CTA exits only after every MMA it issued has completed
+            mma_commit(b_mdone);  // the CTA exits only after every MMA it issued has completed
             mbar_wait(b_mdone, 0, clock64() + kDrainCycles);
         }
     } else {
-        // ---------------------------------------------------------------- dequant + epilogue
+        // ---------------------------------------------------------------- dequant + epilogue (warps 2 .. kXWarp-1)
         const int set = (warp - 2) >> 2;
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
         const int i = quarter * 32 + lane;        // MMA row
@@ -436,13 +497,14 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                     ok = false;
                     break;
                 }
+                const int h = kb & 1;  // sub-stage: A columns 32h .. 32h + 31 of the stage's slot
                 if ((q & (kSets - 1)) == set) {
-                    if (around > 0 && !warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline)) {
+                    if (h == 0 && around > 0 && !warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline)) {
                         record_error(27);
                         ok = false;
                         break;
                     }
-                    tc::tc_fence_after();
+                    tc_fence_after();
                     if (warp_ok) {
                         uint32_t out[32];
                         const int g = kb * t.s + sl;
@@ -490,11 +552,13 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
 #pragma unroll
                             for (int w = 0; w < 32; w++) out[w] = 0u;
                         }
-                        tmem_st32(tmem_base + lane_addr + C::kDCols + 32 * aslot, out);
+                        tmem_st32(tmem_base + lane_addr + C::kDCols + 64 * aslot + 32 * h, out);
                     }
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_afull + 8 * aslot);
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(b_afull + 8 * aslot);
+                    }
                 }
                 if (u == U - 1 || kb == t.nt - 1) {  // leaving a load stage
                     __syncwarp();
@@ -512,10 +576,12 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                         sph ^= 1;
                     }
                 }
-                q++;
-                if (++aslot == NA) {
-                    aslot = 0;
-                    around++;
+                if (h == 1) {
+                    q++;
+                    if (++aslot == NA) {
+                        aslot = 0;
+                        around++;
+                    }
                 }
             }
             if (!ok || j % kSets != set) continue;
@@ -525,19 +591,55 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                 ok = false;
                 break;
             }
-            tc::tc_fence_after();
+            tc_fence_after();
             pdl_wait();  // y may still be read by the previous grid (returns at once by now)
-            const int M = P.M, np = P.n[p];
+            const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
             uint16_t* y = P.y[p];
+            if constexpr (C::kWide) {
+                // The x ring is idle now (one tile per CTA, every MMA done): stage the bf16 tile there
+                // as [token][128 rows], then write whole rows of y with 16-byte stores.
+                uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
+                static_assert(C::kXStages * C::kXBytes >= T * 256, "staging tile does not fit the x ring");
+                for (int c = 0; c < T; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_base + lane_addr + c, v);
+#pragma unroll
+                    for (int cc = 0; cc < 32; cc++) stg[(c + cc) * 128 + i] = bf16_bits(__uint_as_float(v[cc]));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_ep + 8 * set);
+                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, deadline)) {
+                    record_error(27);
+                    ok = false;
+                    break;
+                }
+                ep_uses++;
+                if (t.rows == 128 && (np & 7) == 0) {
+                    for (int k = i; k < M * 16; k += 128) {  // token k / 16, 16-byte chunk k % 16
+                        const int tt = k >> 4, cc = k & 15;
+                        *reinterpret_cast<uint4*>(y + static_cast<int64_t>(m0 + tt) * np + t.row0 + 8 * cc) =
+                            *reinterpret_cast<const uint4*>(stg + tt * 128 + 8 * cc);
+                    }
+                } else {
+                    for (int k = i; k < M * t.rows; k += 128) {
+                        const int tt = k / t.rows, rr = k - tt * t.rows;
+                        y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = stg[tt * 128 + rr];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_dfree);
+                continue;
+            }
             float* red = reinterpret_cast<float*>(smem + C::kOffRed);
             const int J = T * t.s;
             for (int c = 0; c < J; c += 16) {
                 uint32_t v[16];
-                tc::tmem_ld16(tmem_base + lane_addr + c, v);
+                tmem_ld16(tmem_base + lane_addr + c, v);
 #pragma unroll
-                for (int a = 1; a < kAcc; a++) {  // add the accumulators in order
+                for (int a = 1; a < C::kAccN; a++) {  // add the accumulators in order
                     uint32_t w[16];
-                    tc::tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
+                    tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
 #pragma unroll
                     for (int cc = 0; cc < 16; cc++) v[cc] = __float_as_uint(__uint_as_float(v[cc]) + __uint_as_float(w[cc]));
                 }
@@ -545,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                 for (int cc = 0; cc < 16; cc++) {
                     const int col = c + cc;
                     if (t.s == 1) {
-                        if (lane_ok && col < M) y[static_cast<int64_t>(col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
+                        if (lane_ok && col < M)
+                            y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
                     } else {
                         const int rel = col - sl;
                         const int tt = rel / t.s;
@@ -553,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                     }
                 }
             }
-            if (t.s > 1) {
+            if (C::kSMax > 1 && t.s > 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_ep + 8 * set);
                 if (!warp_wait(b_ep + 8 * set, ep_uses & 1, deadline)) {
@@ -569,15 +672,15 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
                     y[static_cast<int64_t>(tt) * np + t.row0 + rr] = bf16_bits(acc);
                 }
             }
-            tc::tc_fence_before();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dfree);
         }
     }
-    tc::tc_fence_before();
+    tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        tc::tc_fence_after();
+        tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::kTmemCols)
                      : "memory");
     }
