@@ -119,10 +119,6 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ uint4 lds128(const void* p) {
     uint4 v;
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -162,7 +162,8 @@ struct GemvLayout {
 // metadata, and arms the stage's `full` barrier through cp.async.mbarrier.arrive.  With S > 1 the
 // consumers leave per-slice partial sums in the stage and consumer warp 0 adds them in slice order.
 // Every wait is bounded; after a timeout the waiting thread records an error code and stops.
-template <int MT, int LPG>
+// RMAX bounds the rows a consumer warp takes per block (the launcher picks R <= RMAX).
+template <int MT, int LPG, int RMAX>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K,
                 const GemvLayout L, uint32_t m1, uint32_t p16) {
@@ -170,7 +171,6 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     constexpr int CB = WPL / 2;        // code bytes per consumer lane per row
     constexpr int CHUNKS = CB / 16;
     constexpr int GPW = 32 / LPG;      // groups per slice
-    constexpr int RMAX = 2;  // rows per consumer warp per block (the launcher picks 1 or 2)
     constexpr int V = pow2_ceil(RMAX * MT);
     extern __shared__ __align__(16) uint8_t smem[];
 
@@ -203,14 +203,10 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 
     if (warp == C) {
         // ------------------------------------------------------------------ producer
-        if (my_blocks > 0) {  // warm L2 with the first block before waiting for the previous grid
-            const int64_t r = static_cast<int64_t>(blockIdx.x) * L.RB + lane;
-            if (lane < L.RB && r < N) {
-                const int pp = problem_of(P, r);
-                prefetch_l2(P.codes[pp] + (r - P.row0[pp]) * static_cast<int64_t>(K / 2));
-            }
-        }
-        pdl_wait();
+        // The producer moves weights only (codes, scales, row metadata into shared memory), which
+        // the previous grid in the stream does not write: it starts at once, without the
+        // programmatic-dependent-launch wait, so that the first blocks arrive while that grid's last
+        // CTAs finish.  The consumers wait for it before they read x and write y.
         // Lane j copies rows j, j + 32, ... of the block: each row's codes with one bulk copy
         // (transaction bytes on the stage's `full` barrier) and its scale window with zero-filling
         // 16-byte copies.  Every row of the block gets its metadata (valid = 0 past the end).
@@ -383,7 +379,7 @@ struct TableState {
 };
 TableState g_tables;
 
-template <int MT, int LPG>
+template <int MT, int LPG, int RMAX>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
     constexpr int CB = kGroup / LPG / 2;
     constexpr int GPW = 32 / LPG;
@@ -391,8 +387,10 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     const int G = static_cast<int>(K / kGroup);
     GemvLayout L = {};
     L.S = (G + GPW - 1) / GPW;
-    // Rows per consumer warp: 2 for large matrices, 1 when that leaves SMs idle.
-    L.R = (N >= static_cast<int64_t>(2) * kMaxWarps * num_sms) ? 2 : 1;
+    // Rows per consumer warp: RMAX whenever K spans several slices (a lane then holds one group per
+    // row, and more rows multiply the independent work per block), else 2 for large matrices and 1
+    // when two would leave SMs idle.
+    L.R = L.S > 1 ? RMAX : (N >= static_cast<int64_t>(2) * kMaxWarps * num_sms ? 2 : 1);
     int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
     const int qmax = L.S >= kMaxWarps ? 1 : kMaxWarps / L.S;
     L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
@@ -416,7 +414,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     cudaGetDevice(&dev);
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG, RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -430,7 +428,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG>, x, P, static_cast<int>(K), L, 0xFFFFFFFFu, 0x10000u);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, RMAX>, x, P, static_cast<int>(K), L, 0xFFFFFFFFu, 0x10000u);
 }
 
 }  // namespace
@@ -665,10 +663,12 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
     P.row0[count] = static_cast<int>(rows);
     for (int i = count + 1; i <= kMaxGroup; i++) P.row0[i] = P.row0[count];
     switch (M) {
-        case 1: return launch_gemv_t<1, 1>(x, P, K, num_sms, stream);
-        case 2: return launch_gemv_t<2, 2>(x, P, K, num_sms, stream);
-        case 3: return launch_gemv_t<3, 2>(x, P, K, num_sms, stream);
-        case 4: return launch_gemv_t<4, 2>(x, P, K, num_sms, stream);
+        case 1:  // K past one slice (32 groups): four rows per warp, else up to two
+            return K > 32 * kGroup ? launch_gemv_t<1, 1, 4>(x, P, K, num_sms, stream)
+                                   : launch_gemv_t<1, 1, 2>(x, P, K, num_sms, stream);
+        case 2: return launch_gemv_t<2, 2, 2>(x, P, K, num_sms, stream);
+        case 3: return launch_gemv_t<3, 2, 2>(x, P, K, num_sms, stream);
+        case 4: return launch_gemv_t<4, 2, 2>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }
