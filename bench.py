@@ -220,7 +220,7 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": decode_traffic_per_launch(),
                      "algorithmic_bytes_per_launch": int(algo / launches),
-                     "kernel": "gemv_kernel<1,1>",
+                     "kernel": "gemv_kernel<1,1,2|4> (CUDA-core GEMV, M = 1)",
                      "note": "algorithmic bytes (codes+scales+x+y) per launch / average launch time over the "
                              "timed steps, inter-launch gaps included; peak of measured"},
         "e2e": {"value": round(packed / e2e_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -266,6 +266,7 @@ def prefill_bench(nf4, synth, dev, pk):
         tf = flops / t / 1e12
         packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, _, _ in mats.values())
         out[f"M{m}"] = {"tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                        "kernel": f"stream_kernel<{32 if m <= 32 else 256}> (tcgen05, dequant into tensor memory)",
                         "packed_gbs": round(packed / t / 1e9, 1), "ms": round(t * 1e3, 4),
                         "clocks": clocks_summary(samples)}
     return out
