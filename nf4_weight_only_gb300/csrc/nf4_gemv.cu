@@ -41,16 +41,12 @@ constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 // out in blocks of eight: the eight low-byte chunks, then the eight high-byte chunks, so the chunk
 // of row m sits at index m + (m & ~7) (+ 8 for the high bytes) and eight lanes reading random rows
 // spread over all eight 16-byte bank groups of a 128-byte line.
-// Rows 1024..2047 repeat the table at twice the value (V[m][c] * 2, exact), which the tensor-core
-// path uses to fold an odd scale exponent into the table.
-__device__ uint4 g_vtab[2048 * 2];
+__device__ uint4 g_vtab[2048];
 
 __global__ void build_vtab_kernel() {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;  // table row: 1024 * p + mantissa class
-    if (m >= 2048) return;
-    // (1 + (m mod 1024)/1024) * 2^(m / 1024), exactly
-    const float s1 = __uint_as_float((0x3F800000u + (static_cast<uint32_t>(m >> 10) << 23)) |
-                                     (static_cast<uint32_t>(m & 1023) << 13));
+    const int m = blockIdx.x * blockDim.x + threadIdx.x;  // mantissa class of the scale
+    if (m >= 1024) return;
+    const float s1 = __uint_as_float(0x3F800000u | (static_cast<uint32_t>(m) << 13));  // 1 + m/1024
     uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int c = 0; c < 16; c++) {
@@ -635,7 +631,7 @@ cudaError_t ensure_tables(int device, cudaStream_t stream) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_tables.mu);
     if (g_tables.ready[device]) return cudaSuccess;
-    build_vtab_kernel<<<8, 256, 0, stream>>>();
+    build_vtab_kernel<<<4, 256, 0, stream>>>();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // One-time wait so that later calls on any stream see the table.

@@ -34,8 +34,9 @@
 // Weights do not depend on the previous kernel in the stream, so warp 0 never waits for it; only x
 // and y do.  Each producer runs as far ahead as its own ring allows.
 //
-// The V table is the 1024-row half (32 KB) of the per-device table: an odd scale exponent is folded
-// in registers instead (flip the exponent's low bit in the low byte, carry into the high byte).
+// The per-device V table (32 KB, see nf4_gemv.cu) gives V[m][c] = bf16(T[c] * (1 + m/1024)); the
+// scale's exponent is added in registers (an odd exponent flips the exponent's low bit in the low
+// byte and carries into the high byte; the rest is added to the high byte).
 // Every mbarrier wait is bounded; a wait that runs out records an error code, drains the copies and
 // MMAs in flight (bounded again) and frees tensor memory.
 #pragma once
