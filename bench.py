@@ -47,6 +47,20 @@ def decode_traffic_per_launch():
         return None
 
 
+def max_over_ranks(seconds: float, device) -> float:
+    """The slowest rank's time (all ranks call it; device is where the process group's tensors live:
+    the rank's GPU for NCCL, the CPU for gloo)."""
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job rate: the units every rank processed (weak scaling: each rank runs its own replica)
+    divided by the slowest rank's time."""
+    return units_per_rank_step * steps * world / max_seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -169,12 +183,10 @@ def run_ours(args, rank, world):
     times, total_s, samples = timed_replays(graph, stream, args.steps, args.warmup, dev.index)
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+        total_s = max_over_ranks(total_s, dev)
     clocks = clocks_summary(samples)
     step_s = statistics.median(times)
-    gbs = packed * args.steps * world / total_s / 1e9
+    gbs = job_throughput(packed, args.steps, world, total_s) / 1e9
     per_launch_s = total_s / args.steps / launches
     achieved = (algo / launches) / per_launch_s / 1e9
 
