@@ -219,6 +219,7 @@ def run_ours(args, rank, world):
     d2h = sum(2 * y.numel() for y in y_list)
 
     prefill = prefill_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
+    embed = embed_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
 
     result = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -242,7 +243,43 @@ def run_ours(args, rank, world):
     }
     if prefill is not None:
         result["prefill"] = prefill
+    if embed is not None:
+        result["embed"] = embed
     return result
+
+
+def embed_bench(nf4, synth, dev, pk, vocab: int = 151936, hidden: int = 2048, n_ids: int = 4096):
+    """GB/s of `nf4_embed` gathering `n_ids` random rows of a 3B-shaped packed embedding table
+    (ids read, codes and scales of each row read, bf16 rows written)."""
+    w = synth.device_weights(31, vocab, hidden, dev)
+    codes, scales = nf4.quantize(w)
+    del w
+    gen = torch.Generator(device="cpu").manual_seed(32)
+    ids = torch.randint(0, vocab, (n_ids,), generator=gen, dtype=torch.int32).to(dev)
+    out = torch.empty((n_ids, hidden), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2, written before each launch
+    iters = 50
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            nf4.nf4_embed(ids, codes, scales, out, stream)
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            nf4.nf4_embed(ids, codes, scales, out, stream)
+            b.record(stream)
+    samples = []
+    while not evs[-1][1].query():
+        samples.append(sample_clocks(dev.index))
+    torch.cuda.synchronize()
+    t = statistics.median(a.elapsed_time(b) / 1e3 for a, b in evs)
+    algo = n_ids * (4 + hidden // 2 + hidden // 64 * 2 + 2 * hidden)
+    gbs = algo / t / 1e9
+    return {"workload": f"{n_ids} random ids of a {vocab} x {hidden} packed table", "gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "us": round(t * 1e6, 2),
+            "algorithmic_bytes": algo, "kernel": "embed_kernel", "l2": "flushed (256 MB written) before each launch",
+            "clocks": clocks_summary(samples)}
 
 
 def prefill_bench(nf4, synth, dev, pk):
@@ -354,7 +391,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill and embedding lines")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--profile-linear", nargs=3, type=int, metavar=("M", "N", "K"),
                     help="run one M x N x K linear four times (for single-kernel profiler captures) and exit")

@@ -115,11 +115,28 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
                               cudaStream_t stream);
 
 /*
- * nf4_check_device_error - diagnostics: read and clear the device-side error word of the current
- * device.  The tensor-core path bounds every pipeline wait (about one second); a wait that runs
- * out records a nonzero code there, and the kernel drains and exits instead of hanging.  *code
- * receives that code (0 = none).  This call waits for the device (it is not meant for the hot
- * path).
+ * nf4_embed - rows of a packed embedding table, dequantized on request (deep-fold README, overview
+ * paragraph: embeddings reconstruct only the rows that are asked for; the 20B run of its results
+ * uses these packed embedding rows).  The table has the same format as a linear's weights: V rows
+ * of K dimensions, groups of 64 along K with one FP16 scale each.
+ *   ids     in   int32 [n_ids]; each should be in [0, V)
+ *   codes   in   uint8 [V][K/2]
+ *   scales  in   fp16 bits [V][K/64]
+ *   out     out  bf16 bits [n_ids][K], out[i][k] = bf16_rn(fp32(T[code] * float(scale))) of row ids[i]
+ *            (bit for bit the rows nf4_dequant would write); must not overlap ids, codes or scales
+ * An id outside [0, V) gives a row of zeros and records code 41 in the device error word (see
+ * nf4_check_device_error); nothing is read for it.  n_ids = 0 is a no-op.  Other errors as for
+ * nf4_dequant.
+ */
+nf4_status nf4_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
+                     int64_t K, uint16_t* out, cudaStream_t stream);
+
+/*
+ * nf4_check_device_error - diagnostics: read and clear the device-side error words of the current
+ * device.  The linear kernels bound every pipeline wait (about one second); a wait that runs out
+ * records a nonzero code (1..39), and the kernel drains and exits instead of hanging.  nf4_embed
+ * records 41 for an id outside the table.  *code receives the first recorded code (0 = none).
+ * This call waits for the device (it is not meant for the hot path).
  */
 nf4_status nf4_check_device_error(int* code);
 

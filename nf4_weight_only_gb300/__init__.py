@@ -22,8 +22,8 @@ STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_
                 4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA"}
 
 # Every symbol include/nf4.h declares.
-EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_check_device_error",
-            "nf4_status_str", "nf4_abi_version")
+EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_embed",
+            "nf4_check_device_error", "nf4_status_str", "nf4_abi_version")
 
 
 class NF4Error(RuntimeError):
@@ -54,6 +54,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_linear.restype = ci
     lib.nf4_linear_grouped.argtypes = [vp, i64, i64, ci, vp, vp, vp, vp, vp]
     lib.nf4_linear_grouped.restype = ci
+    lib.nf4_embed.argtypes = [vp, i64, vp, vp, i64, i64, vp, vp]
+    lib.nf4_embed.restype = ci
     lib.nf4_status_str.argtypes = [ci]
     lib.nf4_status_str.restype = ctypes.c_char_p
     lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -128,6 +130,13 @@ def nf4_linear_grouped(x: torch.Tensor, codes, scales, ys, stream=None) -> None:
                                      ctypes.cast(ns, ctypes.c_void_p), _stream(stream)), "nf4_linear_grouped")
 
 
+def nf4_embed(ids: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """out[i] = w_hat[ids[i]] for int32 ids, codes [V, K/2], scales [V, K/64] -> out bf16 [n, K]."""
+    v, k = codes.shape[0], codes.shape[1] * 2
+    _check(load().nf4_embed(_ptr(ids), ids.numel(), _ptr(codes), _ptr(scales), v, k, _ptr(out), _stream(stream)),
+           "nf4_embed")
+
+
 def nf4_check_device_error() -> int:
     """Read and clear the device error word (0 = no pipeline wait timed out).  Synchronizes."""
     code = ctypes.c_int(0)
@@ -148,6 +157,12 @@ def dequant(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Ten
     w_hat = torch.empty((codes.shape[0], codes.shape[1] * 2), dtype=torch.bfloat16, device=codes.device)
     nf4_dequant(codes, scales, w_hat, stream)
     return w_hat
+
+
+def embed(ids: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:
+    out = torch.empty((ids.numel(), codes.shape[1] * 2), dtype=torch.bfloat16, device=codes.device)
+    nf4_embed(ids, codes, scales, out, stream)
+    return out
 
 
 def linear(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:

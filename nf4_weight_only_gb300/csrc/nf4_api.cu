@@ -143,7 +143,27 @@ nf4_status nf4_check_device_error(int* code) {
     int dev = 0, sms = 0;
     nf4_status st = current_device(&dev, &sms);
     if (st != NF4_OK) return st;
-    return from_cuda(nf4::read_and_clear_error(code));
+    int linear = 0, embed = 0;
+    if ((st = from_cuda(nf4::read_and_clear_error(&linear))) != NF4_OK) return st;
+    if ((st = from_cuda(nf4::read_and_clear_embed_error(&embed))) != NF4_OK) return st;
+    *code = linear ? linear : embed;
+    return NF4_OK;
+}
+
+nf4_status nf4_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
+                     int64_t K, uint16_t* out, cudaStream_t stream) {
+    if (n_ids < 0 || V < 0 || n_ids > kMaxDim || V > kMaxDim) return NF4_ERR_SHAPE;
+    nf4_status st = check_k(K);
+    if (st != NF4_OK) return st;
+    if (n_ids == 0) return NF4_OK;
+    if (!ids || !out || (V > 0 && (!codes || !scales))) return NF4_ERR_NULL;
+    if (!aligned16(ids) || !aligned16(out) || (V > 0 && (!aligned16(codes) || !aligned16(scales))))
+        return NF4_ERR_ALIGN;
+    const int64_t ob = n_ids * K * 2, ib = n_ids * 4, cb = V * K / 2, sb = V * (K / NF4_GROUP_SIZE) * 2;
+    if (overlap(out, ob, ids, ib) || overlap(out, ob, codes, cb) || overlap(out, ob, scales, sb)) return NF4_ERR_ALIAS;
+    int dev = 0, sms = 0;
+    if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
+    return from_cuda(nf4::launch_embed(ids, n_ids, codes, scales, V, K, out, sms, stream));
 }
 
 nf4_status nf4_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes, uint16_t* scales,

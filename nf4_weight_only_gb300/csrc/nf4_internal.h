@@ -28,8 +28,13 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
 cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* codes, const uint16_t* const* scales,
                           uint16_t* const* ys, const int64_t* Ns, int64_t M, int64_t K, int num_sms,
                           cudaStream_t stream);
-// Device error word of the tensor-core path (nonzero after a bounded pipeline wait timed out).
+// Device error word of the linear kernels (nonzero after a bounded pipeline wait timed out).
 cudaError_t read_and_clear_error(int* code);
+
+// Packed embedding rows (out-of-range ids write zeros and set the embed error word to 41).
+cudaError_t launch_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
+                         int64_t K, uint16_t* out, int num_sms, cudaStream_t stream);
+cudaError_t read_and_clear_embed_error(int* code);
 
 // Per-device constant table used by the GEMV (built once per device, stream-ordered).
 cudaError_t ensure_tables(int device, cudaStream_t stream);

@@ -101,6 +101,45 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
     }
 }
 
+// Error word of nf4_embed (41: an id outside the table).
+__device__ int g_embed_error;
+
+// Packed embedding rows: thread per quarter group (16 weights) of a requested row, the same exact
+// arithmetic as dequant_kernel; an id outside [0, V) writes zeros and records 41.
+__global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids, int64_t n_ids,
+                                                    const uint8_t* __restrict__ codes,
+                                                    const uint16_t* __restrict__ scales, int64_t V, int64_t K,
+                                                    uint16_t* __restrict__ out) {
+    __shared__ float table[16];
+    if (threadIdx.x < 16) table[threadIdx.x] = kNF4[threadIdx.x];
+    __syncthreads();
+    const int64_t qpr = K / 16;  // quarter groups per row
+    const int64_t quarters = n_ids * qpr;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < quarters; q += stride) {
+        const int64_t i = q / qpr, qq = q - i * qpr;
+        const int64_t id = ids[i];
+        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (id >= 0 && id < V) {
+            const int64_t src = id * qpr + qq;  // quarter index inside the table
+            const uint2 cw = *(reinterpret_cast<const uint2*>(codes) + src);
+            const float s = __half2float(__ushort_as_half(scales[src >> 2]));
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t byte = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
+                const uint32_t lo = bf16_bits(__fmul_rn(table[byte & 0xFu], s));
+                const uint32_t hi = bf16_bits(__fmul_rn(table[byte >> 4], s));
+                o[j] = lo | (hi << 16);
+            }
+        } else if (qq == 0) {
+            atomicCAS(&g_embed_error, 0, 41);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + q * 16);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 int grid_for(int64_t items_per_block_units, int64_t units, int num_sms, int blocks_per_sm) {
     int64_t blocks = (units + items_per_block_units - 1) / items_per_block_units;
     int64_t cap = static_cast<int64_t>(num_sms) * blocks_per_sm;
@@ -127,6 +166,25 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t
     const int grid = grid_for(256, groups * 4, num_sms, 8);
     dequant_kernel<<<grid, 256, 0, stream>>>(codes, scales, groups, w_hat);
     return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
+                         int64_t K, uint16_t* out, int num_sms, cudaStream_t stream) {
+    const int64_t quarters = n_ids * (K / 16);
+    if (quarters == 0) return cudaSuccess;
+    const int grid = grid_for(256, quarters, num_sms, 8);
+    embed_kernel<<<grid, 256, 0, stream>>>(ids, n_ids, codes, scales, V, K, out);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_embed_error(int* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_embed_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_embed_error, &zero, sizeof(int));
+    *code = v;
+    return e;
 }
 
 }  // namespace nf4

@@ -66,6 +66,8 @@ class Oracle:
         lib.oracle_quantize.restype = ctypes.c_int
         lib.oracle_dequant.argtypes = [vp, vp, i64, i64, vp]
         lib.oracle_dequant.restype = ctypes.c_int
+        lib.oracle_embed.argtypes = [vp, i64, vp, vp, i64, i64, vp]
+        lib.oracle_embed.restype = i64
         lib.oracle_linear.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, ctypes.c_int]
         lib.oracle_linear.restype = ctypes.c_int
         lib.oracle_linear_entries.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, vp]
@@ -119,6 +121,18 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_dequant: bad shape")
         return out
+
+    def embed(self, ids: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> Tuple[np.ndarray, int]:
+        """int32 ids [n] of a V-row table -> (bf16 bits u16 [n, K], number of ids outside [0, V))."""
+        ids = np.ascontiguousarray(ids, np.int32)
+        codes = np.ascontiguousarray(codes, np.uint8)
+        scales = np.ascontiguousarray(scales, np.uint16)
+        v, k = codes.shape[0], codes.shape[1] * 2
+        out = np.empty((ids.size, k), np.uint16)
+        bad = self.lib.oracle_embed(_p(ids), ids.size, _p(codes), _p(scales), v, k, _p(out))
+        if bad < 0:
+            raise ValueError("oracle_embed: bad shape")
+        return out, int(bad)
 
     def linear(self, x_bf16: np.ndarray, codes: np.ndarray, scales: np.ndarray,
                nthreads: int = 1) -> Tuple[np.ndarray, np.ndarray]:

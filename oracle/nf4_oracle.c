@@ -16,6 +16,8 @@
  *   - deep-fold README, execution-path table: the linear kernels dequantize only the current tile
  *     and never write a dense weight matrix back; decode is an N=1 GEMV, prefill a GEMM of up to 32
  *     positions.
+ *   - deep-fold README, overview paragraph: embeddings (PackedEmbed) reconstruct only the rows that
+ *     are requested.
  *   The rest is the library's own pinned reading of what the pages leave open: absmax scale per
  *   group (fp32 max, stored as fp16 round-to-nearest-even), code = argmin_i |fp32(w/s) - T[i]| in
  *   fp32 with ties to the lower index, two codes per byte with the low nibble first, dequantized
@@ -215,6 +217,27 @@ int oracle_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int6
         for (int64_t k = 0; k < K; k++)
             w_hat[n * K + k] = dequant_value(code_at(codes, K, n, k), scales[n * G + k / NF4_GROUP]);
     return 0;
+}
+
+/* Packed embedding rows (deep-fold README, overview paragraph: embeddings reconstruct only the
+ * requested rows): out[i][k] = the dequantized weight (ids[i], k) of a V x K table; an id outside
+ * [0, V) gives a row of zeros (the library's reading; the pages do not say).  Returns the number of
+ * such ids. */
+int64_t oracle_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
+                     int64_t K, uint16_t* out) {
+    if (n_ids < 0 || V < 0 || K <= 0 || K % NF4_GROUP != 0) return -1;
+    int64_t G = K / NF4_GROUP, bad = 0;
+    for (int64_t i = 0; i < n_ids; i++) {
+        int64_t id = ids[i];
+        for (int64_t k = 0; k < K; k++) {
+            if (id < 0 || id >= V)
+                out[i * K + k] = 0;
+            else
+                out[i * K + k] = dequant_value(code_at(codes, K, id, k), scales[id * G + k / NF4_GROUP]);
+        }
+        if (id < 0 || id >= V) bad++;
+    }
+    return bad;
 }
 
 /* ------------------------------------------------------------------------------------------------

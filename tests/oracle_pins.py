@@ -392,5 +392,25 @@ def pin_linear(o):
     assert np.array_equal(y1, y64)
 
 
+def pin_embed(o):
+    """Packed embedding rows against numpy's gather of the (exhaustively pinned) dequantized table;
+    ids outside the table give zero rows and are counted."""
+    from nf4_weight_only_gb300 import synth
+    v, k = 37, 192
+    codes, scales = o.quantize(synth.weights(12, v, k))
+    table = o.dequant(codes, scales)
+    rng = np.random.default_rng(13)
+    ids = np.concatenate([[0, v - 1, 5, 5], rng.integers(0, v, 60)]).astype(np.int32)
+    rows, bad = o.embed(ids, codes, scales)
+    assert bad == 0 and np.array_equal(rows, table[ids])
+    assert np.array_equal(rows[2], rows[3])  # a repeated id gives the same row
+    odd = np.array([3, -1, v, 2 ** 31 - 1, v - 1], np.int32)
+    rows, bad = o.embed(odd, codes, scales)
+    assert bad == 3
+    assert np.array_equal(rows[[0, 4]], table[[3, v - 1]]) and not rows[1:4].any()
+    rows, bad = o.embed(np.zeros(0, np.int32), codes, scales)
+    assert rows.shape == (0, k) and bad == 0
+
+
 FAST_PINS = [pin_table, pin_f16, pin_bf16, pin_code_windows, pin_quantize_exact, pin_golden_pack,
-             pin_payload_ratio, pin_dequant_exhaustive, pin_roundtrip, pin_linear]
+             pin_payload_ratio, pin_dequant_exhaustive, pin_roundtrip, pin_linear, pin_embed]

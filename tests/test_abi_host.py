@@ -126,3 +126,20 @@ def test_grouped_validation(lib):
     assert args(A, 1, 64, 2, c2, s2, arr(D, D + 16), ns) == 4  # y0 (32 bytes) and y1 overlap
     assert args(A, 1, 64, 2, c2, s2, arr(D, B + 16), ns) == 4  # y1 inside codes[0]
     assert args(A, 0, 64, 2, c2, s2, y2, ns) == 0          # empty
+
+
+def test_embed_validation(lib):
+    e = lib.nf4_embed
+    e.argtypes = [vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64, vp, vp]
+    assert e(vp(0), 0, vp(0), vp(0), 0, 64, vp(0), None) == 0          # no ids: no-op
+    assert e(vp(A), 4, vp(B), vp(C), 10, 100, vp(D), None) == 2        # K not a multiple of 64
+    assert e(vp(A), -1, vp(B), vp(C), 10, 64, vp(D), None) == 2
+    assert e(vp(A), 4, vp(B), vp(C), -1, 64, vp(D), None) == 2
+    assert e(vp(0), 4, vp(B), vp(C), 10, 64, vp(D), None) == 1        # ids NULL
+    assert e(vp(A), 4, vp(0), vp(C), 10, 64, vp(D), None) == 1        # codes NULL
+    assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(0), None) == 1        # out NULL
+    assert e(vp(A + 4), 4, vp(B), vp(C), 10, 64, vp(D), None) == 3
+    assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(D + 2), None) == 3
+    assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(A), None) == 4         # out over ids
+    assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(B + 32), None) == 4    # out inside codes
+    assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(C), None) == 4         # out over scales

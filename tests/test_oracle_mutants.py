@@ -43,6 +43,11 @@ MUTANTS = [
      "double p = (k == K - 1) ? 0.0 : xrow[k] * wrow[k];"),
     ("linear subtracts", "acc += p;\n                mag += fabs(p);", "acc -= p;\n                mag += fabs(p);"),
     ("linear magnitude without abs", "acc += p;\n                mag += fabs(p);", "acc += p;\n                mag += p;"),
+    ("embed reads the row of the position, not of the id",
+     "out[i * K + k] = dequant_value(code_at(codes, K, id, k), scales[id * G + k / NF4_GROUP]);",
+     "out[i * K + k] = dequant_value(code_at(codes, K, i % V, k), scales[(i % V) * G + k / NF4_GROUP]);"),
+    ("embed writes ones for an id outside the table", "if (id < 0 || id >= V)\n                out[i * K + k] = 0;",
+     "if (id < 0 || id >= V)\n                out[i * K + k] = 0x3F80;"),
 ]
 
 

@@ -356,3 +356,71 @@ def test_linear_stream_long_k(nf4, o, m, n, k):
     """M <= 4 with K past the GEMV's register-resident range runs the streaming kernel."""
     check_linear(nf4, o, m, n, k, seed=11 * n + k + m)
     assert device_error(nf4) == 0
+
+
+# ------------------------------------------------------------------------------------------------
+# packed embedding rows
+# ------------------------------------------------------------------------------------------------
+def run_embed(nf4, ids, codes_d, scales_d, k):
+    out = Guarded((len(ids), k), torch.bfloat16)
+    nf4.nf4_embed(torch.from_numpy(np.asarray(ids, np.int32)).to(DEV), codes_d, scales_d, out.t)
+    torch.cuda.synchronize()
+    assert out.canaries_intact(), "nf4_embed wrote outside out"
+    return dev_to_bits(out.t)
+
+
+def test_embed_bit_exact(nf4, o):
+    from nf4_weight_only_gb300 import synth
+    v, k = 1000, 2048
+    codes, scales = o.quantize(synth.weights(21, v, k))
+    cd = torch.from_numpy(codes).to(DEV)
+    sd = torch.from_numpy(scales.view(np.int16)).view(torch.float16).to(DEV)
+    rng = np.random.default_rng(22)
+    ids = np.concatenate([[0, v - 1, 7, 7], rng.integers(0, v, 300)]).astype(np.int32)
+    got = run_embed(nf4, ids, cd, sd, k)
+    want, bad = o.embed(ids, codes, scales)
+    assert bad == 0 and np.array_equal(got, want)
+    assert device_error(nf4) == 0
+
+
+def test_embed_vocabulary_sampled(nf4, o):
+    """A 3B-shaped vocabulary (151936 x 2048) quantized on the device; 512 sampled ids (with the first
+    and last rows) checked bit for bit against the oracle on those rows."""
+    from nf4_weight_only_gb300 import synth
+    v, k = 151936, 2048
+    codes_d, scales_d = nf4.quantize(synth.device_weights(23, v, k, DEV))
+    rng = np.random.default_rng(24)
+    ids = np.concatenate([[0, v - 1], rng.integers(0, v, 510)]).astype(np.int32)
+    got = run_embed(nf4, ids, codes_d, scales_d, k)
+    uniq, inv = np.unique(ids, return_inverse=True)
+    sel = torch.from_numpy(uniq.astype(np.int64)).to(DEV)
+    c_h = codes_d[sel].cpu().numpy()
+    s_h = scales_d[sel].cpu().view(torch.int16).numpy().view(np.uint16)
+    want, bad = o.embed(inv.astype(np.int32), c_h, s_h)
+    assert bad == 0 and np.array_equal(got, want)
+
+
+def test_embed_out_of_range_ids(nf4, o):
+    from nf4_weight_only_gb300 import synth
+    v, k = 50, 128
+    codes, scales = o.quantize(synth.weights(25, v, k))
+    cd = torch.from_numpy(codes).to(DEV)
+    sd = torch.from_numpy(scales.view(np.int16)).view(torch.float16).to(DEV)
+    assert device_error(nf4) == 0
+    ids = np.array([3, -1, v, 2 ** 31 - 1, v - 1], np.int32)
+    got = run_embed(nf4, ids, cd, sd, k)
+    want, bad = o.embed(ids, codes, scales)
+    assert bad == 3 and np.array_equal(got, want)
+    assert not got[1:4].any()
+    assert device_error(nf4) == 41
+    assert device_error(nf4) == 0  # read and cleared
+
+
+def test_embed_empty_is_noop(nf4):
+    out = torch.full((1, 64), 3.0, dtype=torch.bfloat16, device=DEV)
+    ids = torch.zeros((0,), dtype=torch.int32, device=DEV)
+    codes = torch.zeros((2, 32), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((2, 1), dtype=torch.float16, device=DEV)
+    nf4.nf4_embed(ids, codes, scales, out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
