@@ -220,6 +220,7 @@ def run_ours(args, rank, world):
 
     prefill = prefill_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
     embed = embed_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
+    overflow = overflow_bench(nf4, synth, dev) if not args.skip_prefill else None
 
     result = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -245,7 +246,65 @@ def run_ours(args, rank, world):
         result["prefill"] = prefill
     if embed is not None:
         result["embed"] = embed
+    if overflow is not None:
+        result["overflow"] = overflow
     return result
+
+
+def overflow_bench(nf4, synth, dev, layers: int = 2, passes: int = 8):
+    """Overflow streaming: `layers` 32B-shaped layers (7 linears each, M = 1) whose packed weights
+    stay in pinned host memory, streamed through the two-slot ring.  Reported as packed GB/s
+    against a plain host-to-device copy of the same bytes (the link's own rate)."""
+    wl = W.SWEEP_32B
+    mats = []
+    for layer in range(layers):
+        for li, lin in enumerate(wl.linears):
+            w = synth.device_weights(wl.seed * 100003 + layer * 16 + li, lin.n, lin.k, dev)
+            codes, scales = nf4.quantize(w)
+            del w
+            mats.append((lin, codes.cpu().pin_memory(), scales.cpu().pin_memory()))
+            del codes, scales
+    torch.cuda.synchronize()
+    xs = {k: synth.device_activations_bf16(88 + k, 1, k, dev) for k in {l.k for l in wl.linears}}
+    ys = [torch.empty((1, lin.n), dtype=torch.bfloat16, device=dev) for lin, _, _ in mats]
+    ops = [(xs[lin.k], c, s, y) for (lin, c, s), y in zip(mats, ys)]
+    packed = sum(c.numel() + 2 * s.numel() for _, c, s in mats)
+    stream = torch.cuda.Stream(device=dev)
+    ring = nf4.Ring(max(nf4.Ring.bytes_needed(lin.n, lin.k) for lin in wl.linears))
+    try:
+        for _ in range(2):
+            ring.run(ops, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(passes):
+            ring.run(ops, stream)
+        e1.record(stream)
+        samples = []
+        while not e1.query():
+            samples.append(sample_clocks(dev.index))
+        torch.cuda.synchronize()
+        ring_s = e0.elapsed_time(e1) / 1e3 / passes
+    finally:
+        ring.close()
+    # the link alone: one pinned buffer of the same size copied to the device
+    host = torch.empty(packed, dtype=torch.uint8).pin_memory()
+    devbuf = torch.empty(packed, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        devbuf.copy_(host, non_blocking=True)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(passes):
+            devbuf.copy_(host, non_blocking=True)
+        c1.record(stream)
+    torch.cuda.synchronize()
+    copy_s = c0.elapsed_time(c1) / 1e3 / passes
+    return {"workload": f"{layers} x 32B-shaped layer ({len(mats)} linears, M = 1) from pinned host memory",
+            "packed_bytes_per_pass": packed, "gbs": round(packed / ring_s / 1e9, 1), "ms_per_pass": round(ring_s * 1e3, 3),
+            "h2d_copy_gbs": round(packed / copy_s / 1e9, 1), "frac_of_h2d_copy": round(copy_s / ring_s, 4),
+            "kernel": "nf4_ring_run (copy engine into two slots + the linear kernels)",
+            "clocks": clocks_summary(samples)}
 
 
 def embed_bench(nf4, synth, dev, pk, vocab: int = 151936, hidden: int = 2048, n_ids: int = 4096):

@@ -21,7 +21,8 @@
  *   - Pointers are device pointers owned by the caller, row-major and contiguous, each aligned to
  *     16 bytes.  bf16 and fp16 values travel as their 16-bit patterns (uint16_t).
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream).  No call synchronises
- *     the device, allocates memory or keeps state beyond a per-device capability check.
+ *     the device, allocates memory or keeps state beyond a per-device capability check, except the
+ *     ring calls of the overflow-streaming section, which own explicitly created state.
  *   - Arguments are checked on the host before anything is launched; on an error nothing is
  *     launched and no output is written.  A failed launch returns NF4_ERR_CUDA and leaves the CUDA
  *     error state cleared.
@@ -42,7 +43,7 @@ extern "C" {
 #endif
 
 #define NF4_GROUP_SIZE 64
-#define NF4_ABI_VERSION 1
+#define NF4_ABI_VERSION 2
 
 typedef enum nf4_status {
     NF4_OK = 0,
@@ -51,7 +52,9 @@ typedef enum nf4_status {
     NF4_ERR_ALIGN = 3,              /* a pointer is not 16-byte aligned */
     NF4_ERR_ALIAS = 4,              /* an output range overlaps an input range */
     NF4_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 (sm_103) */
-    NF4_ERR_CUDA = 6                /* a CUDA runtime call or kernel launch failed */
+    NF4_ERR_CUDA = 6,               /* a CUDA runtime call or kernel launch failed */
+    NF4_ERR_MEMORY = 7              /* memory of the wrong kind: a host pointer that is not page-locked,
+                                       or a ring used on a device other than its own */
 } nf4_status;
 
 /*
@@ -130,6 +133,60 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
  */
 nf4_status nf4_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
                      int64_t K, uint16_t* out, cudaStream_t stream);
+
+/*
+ * Overflow streaming (deep-fold README, overview and execution-path table: a model larger than the
+ * card keeps part of its packed weights in pinned host memory and copies them through two reusable
+ * device slots, overlapped with the same GEMV / GEMM; the 32B row of its results runs this way).
+ *
+ * A ring is the one stateful object of the library: two device slots, a copy stream and events,
+ * created on the current device.  nf4_ring_run walks a list of linears whose packed weights live in
+ * page-locked host memory.  Linear i is copied into slot i mod 2 on the ring's copy stream (after
+ * the linear that last read that slot has finished) and then runs as nf4_linear on `stream`, so
+ * the copy of linear i + 1 overlaps the compute of linear i.  The linears run in list order on
+ * `stream`, so the y of one may be the x of a later one.  Results are bit for bit those of
+ * nf4_linear on device-resident copies of the same weights.
+ */
+typedef struct nf4_ring nf4_ring;
+
+/* One linear of a streamed list. */
+typedef struct nf4_host_linear {
+    const uint16_t* x;      /* device, bf16 bits [M][K] */
+    const uint8_t* codes;   /* page-locked host, uint8 [N][K/2] */
+    const uint16_t* scales; /* page-locked host, fp16 bits [N][K/64] */
+    uint16_t* y;            /* device, bf16 bits [M][N]; must not overlap x */
+    int64_t M, N, K;        /* as for nf4_linear; M = 0 or N = 0 skips the entry */
+} nf4_host_linear;
+
+/*
+ * nf4_ring_create - allocate a ring whose two slots hold up to `slot_bytes` of packed weights each:
+ * a linear fits when N*K/2 rounded up to 256, plus N*(K/64)*2, is at most slot_bytes.
+ *   slot_bytes  > 0
+ *   ring        out: the new ring (NULL on error)
+ * Errors: NF4_ERR_NULL, NF4_ERR_SHAPE (slot_bytes <= 0), NF4_ERR_UNSUPPORTED_DEVICE, NF4_ERR_CUDA
+ * (allocation failed; nothing is left allocated).
+ */
+nf4_status nf4_ring_create(int64_t slot_bytes, nf4_ring** ring);
+
+/*
+ * nf4_ring_run - stream `count` linears through the ring, asynchronously on `stream`.
+ *   ring    from nf4_ring_create, used on its own device
+ *   ops     host array of count entries (read before the call returns)
+ *   count   >= 0 (0 is a no-op)
+ * Every entry is checked before anything is enqueued: shapes and alignment as for nf4_linear,
+ * NF4_ERR_SHAPE when an entry does not fit a slot, NF4_ERR_MEMORY when codes or scales are not
+ * page-locked host memory (first and last byte checked) or the current device is not the ring's.
+ * The host buffers must stay unchanged until the work enqueued by the call has finished.  A ring
+ * may be captured into a CUDA graph: a captured run orders its copies after the work already on
+ * `stream`, and so do the ring's eager runs from then on; a graph and eager runs that share a ring
+ * must therefore be issued on one stream (or be ordered by the caller).  Calls on one ring must not run concurrently from several host threads; runs on
+ * different streams are ordered through the ring's events.  A CUDA failure part way returns
+ * NF4_ERR_CUDA with the earlier entries enqueued.
+ */
+nf4_status nf4_ring_run(nf4_ring* ring, const nf4_host_linear* ops, int64_t count, cudaStream_t stream);
+
+/* nf4_ring_destroy - wait for the ring's outstanding work and free it.  NULL is a no-op. */
+nf4_status nf4_ring_destroy(nf4_ring* ring);
 
 /*
  * nf4_check_device_error - diagnostics: read and clear the device-side error words of the current

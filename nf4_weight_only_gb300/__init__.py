@@ -19,11 +19,18 @@ GROUP = 64
 LIB_PATH = _build.LIB_PATH
 
 STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_ALIGN",
-                4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA"}
+                4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA", 7: "NF4_ERR_MEMORY"}
 
 # Every symbol include/nf4.h declares.
 EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_embed",
+            "nf4_ring_create", "nf4_ring_run", "nf4_ring_destroy",
             "nf4_check_device_error", "nf4_status_str", "nf4_abi_version")
+
+
+class HostLinear(ctypes.Structure):
+    """nf4_host_linear: one linear of a streamed list (x, y on the device; codes, scales pinned host)."""
+    _fields_ = [("x", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class NF4Error(RuntimeError):
@@ -56,6 +63,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_linear_grouped.restype = ci
     lib.nf4_embed.argtypes = [vp, i64, vp, vp, i64, i64, vp, vp]
     lib.nf4_embed.restype = ci
+    lib.nf4_ring_create.argtypes = [i64, ctypes.POINTER(ctypes.c_void_p)]
+    lib.nf4_ring_create.restype = ci
+    lib.nf4_ring_run.argtypes = [vp, vp, i64, vp]
+    lib.nf4_ring_run.restype = ci
+    lib.nf4_ring_destroy.argtypes = [vp]
+    lib.nf4_ring_destroy.restype = ci
     lib.nf4_status_str.argtypes = [ci]
     lib.nf4_status_str.restype = ctypes.c_char_p
     lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -135,6 +148,54 @@ def nf4_embed(ids: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, out:
     v, k = codes.shape[0], codes.shape[1] * 2
     _check(load().nf4_embed(_ptr(ids), ids.numel(), _ptr(codes), _ptr(scales), v, k, _ptr(out), _stream(stream)),
            "nf4_embed")
+
+
+def nf4_ring_create(slot_bytes: int) -> int:
+    """A ring of two device slots of `slot_bytes` each (returns the opaque handle)."""
+    h = ctypes.c_void_p(0)
+    _check(load().nf4_ring_create(slot_bytes, ctypes.byref(h)), "nf4_ring_create")
+    return h.value
+
+
+def nf4_ring_run(ring: int, ops, stream=None) -> None:
+    """Stream a list of linears (x, codes, scales, y) through the ring: codes [N, K/2] and scales
+    [N, K/64] in pinned host memory, x [M, K] and y [M, N] on the device."""
+    arr = (HostLinear * max(1, len(ops)))()
+    for i, (x, codes, scales, y) in enumerate(ops):
+        arr[i] = HostLinear(_ptr(x).value, _ptr(codes).value, _ptr(scales).value, _ptr(y).value,
+                            x.shape[0], codes.shape[0], x.shape[1])
+    _check(load().nf4_ring_run(ctypes.c_void_p(ring), ctypes.cast(arr, ctypes.c_void_p), len(ops), _stream(stream)),
+           "nf4_ring_run")
+
+
+def nf4_ring_destroy(ring: int) -> None:
+    _check(load().nf4_ring_destroy(ctypes.c_void_p(ring)), "nf4_ring_destroy")
+
+
+class Ring:
+    """Two reusable device slots through which packed weights in pinned host memory are streamed."""
+
+    def __init__(self, slot_bytes: int):
+        self.handle = nf4_ring_create(slot_bytes)
+        self.slot_bytes = slot_bytes
+
+    @staticmethod
+    def bytes_needed(n: int, k: int) -> int:
+        return (n * k // 2 + 255) // 256 * 256 + n * (k // GROUP) * 2
+
+    def run(self, ops, stream=None) -> None:
+        nf4_ring_run(self.handle, ops, stream)
+
+    def close(self) -> None:
+        if self.handle:
+            nf4_ring_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
 
 
 def nf4_check_device_error() -> int:

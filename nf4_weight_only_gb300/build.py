@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libnf4.so")
 
-SOURCES = ["nf4_api.cu", "nf4_quant.cu", "nf4_gemv.cu"]
+SOURCES = ["nf4_api.cu", "nf4_quant.cu", "nf4_gemv.cu", "nf4_ring.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
                      "-Xptxas", "-warn-spills"]

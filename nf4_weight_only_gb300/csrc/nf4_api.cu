@@ -64,6 +64,10 @@ nf4_status from_cuda(cudaError_t e) {
 
 }  // namespace
 
+namespace nf4 {
+int abi_current_device(int* device, int* sms) { return current_device(device, sms); }
+}  // namespace nf4
+
 extern "C" {
 
 const char* nf4_status_str(nf4_status status) {
@@ -75,6 +79,7 @@ const char* nf4_status_str(nf4_status status) {
         case NF4_ERR_ALIAS: return "NF4_ERR_ALIAS: an output overlaps an input";
         case NF4_ERR_UNSUPPORTED_DEVICE: return "NF4_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
         case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA call or launch failed";
+        case NF4_ERR_MEMORY: return "NF4_ERR_MEMORY: host memory not page-locked, or a ring used on another device";
     }
     return "NF4 status: unknown code";
 }

@@ -39,4 +39,7 @@ cudaError_t read_and_clear_embed_error(int* code);
 // Per-device constant table used by the GEMV (built once per device, stream-ordered).
 cudaError_t ensure_tables(int device, cudaStream_t stream);
 
+// The C-ABI layer's device check (an nf4_status value): the current device and its SM count.
+int abi_current_device(int* device, int* sms);
+
 }  // namespace nf4

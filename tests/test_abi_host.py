@@ -34,8 +34,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.nf4_abi_version() == 1
-    for code in range(7):
+    assert lib.nf4_abi_version() == 2
+    for code in range(8):
         s = lib.nf4_status_str(code).decode()
         assert s.startswith("NF4_")
     assert b"unknown" in lib.nf4_status_str(99)
@@ -143,3 +143,16 @@ def test_embed_validation(lib):
     assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(A), None) == 4         # out over ids
     assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(B + 32), None) == 4    # out inside codes
     assert e(vp(A), 4, vp(B), vp(C), 10, 64, vp(C), None) == 4         # out over scales
+
+
+def test_ring_validation(lib):
+    """Ring calls reject bad arguments before any CUDA call (the ring pointer is never touched)."""
+    h = ctypes.c_void_p(0)
+    assert lib.nf4_ring_create(1 << 20, None) == 1
+    assert lib.nf4_ring_create(0, ctypes.byref(h)) == 2 and h.value is None
+    assert lib.nf4_ring_create(-5, ctypes.byref(h)) == 2
+    assert lib.nf4_ring_run(None, vp(A), 1, None) == 1
+    assert lib.nf4_ring_run(vp(A), vp(B), -1, None) == 2
+    assert lib.nf4_ring_run(vp(A), None, 0, None) == 0   # empty list: no-op
+    assert lib.nf4_ring_run(vp(A), None, 2, None) == 1
+    assert lib.nf4_ring_destroy(None) == 0

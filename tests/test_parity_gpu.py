@@ -424,3 +424,127 @@ def test_embed_empty_is_noop(nf4):
     nf4.nf4_embed(ids, codes, scales, out)
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+# ------------------------------------------------------------------------------------------------
+# overflow streaming through the two-slot ring
+# ------------------------------------------------------------------------------------------------
+def _host_weights(nf4, seed, n, k):
+    """Packed weights quantized on the device; returns (device codes, scales, pinned host copies)."""
+    from nf4_weight_only_gb300 import synth
+    codes, scales = nf4.quantize(synth.device_weights(seed, n, k, DEV))
+    return codes, scales, codes.cpu().pin_memory(), scales.cpu().pin_memory()
+
+
+def test_ring_chain_matches_resident(nf4, o):
+    """Five chained M = 1 linears (y of one is x of the next) of different sizes streamed from
+    pinned host memory: every y is bit for bit the resident nf4_linear result, and the first and
+    last meet the oracle's bound."""
+    from nf4_weight_only_gb300 import synth
+    dims = [2048, 2560, 1024, 2048, 11008, 2048]
+    mats = [_host_weights(nf4, 300 + i, dims[i + 1], dims[i]) for i in range(len(dims) - 1)]
+    x0 = synth.device_activations_bf16(310, 1, dims[0], DEV)
+    ys = [torch.empty((1, n), dtype=torch.bfloat16, device=DEV) for n in dims[1:]]
+    xs = [x0] + ys[:-1]
+    slot = max(nf4.Ring.bytes_needed(dims[i + 1], dims[i]) for i in range(len(mats)))
+    with nf4.Ring(slot) as ring:
+        ring.run([(xs[i], mats[i][2], mats[i][3], ys[i]) for i in range(len(mats))])
+        torch.cuda.synchronize()
+    for i, (cd, sd, _, _) in enumerate(mats):
+        want = torch.empty_like(ys[i])
+        nf4.nf4_linear(xs[i], cd, sd, want)
+        torch.cuda.synchronize()
+        assert torch.equal(want.view(torch.int16), ys[i].view(torch.int16)), f"linear {i}"
+    for i in (0, len(mats) - 1):
+        _, _, ch, sh = mats[i]
+        y64, absum = o.linear(dev_to_bits(xs[i]), ch.numpy(), sh.view(torch.int16).numpy().view(np.uint16),
+                              nthreads=16)
+        ok, ratio, _ = oracle.within_tolerance(dev_to_bits(ys[i]), y64, absum)
+        assert ok, f"oracle bound, linear {i}: worst ratio {ratio:.3f}"
+    assert device_error(nf4) == 0
+
+
+@pytest.mark.parametrize("m", [4, 32])
+def test_ring_small_batch(nf4, m):
+    """M = 4 (GEMV) and M = 32 (tensor-core streaming) through the ring, twelve distinct matrices
+    over two slots, compared with the resident results."""
+    from nf4_weight_only_gb300 import synth
+    n, k = 3072, 2048
+    mats = [_host_weights(nf4, 400 + i, n, k) for i in range(12)]
+    x = synth.device_activations_bf16(401, m, k, DEV)
+    ys = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for _ in mats]
+    with nf4.Ring(nf4.Ring.bytes_needed(n, k)) as ring:
+        ring.run([(x, c[2], c[3], y) for c, y in zip(mats, ys)])
+        torch.cuda.synchronize()
+    for (cd, sd, _, _), y in zip(mats, ys):
+        want = torch.empty_like(y)
+        nf4.nf4_linear(x, cd, sd, want)
+        torch.cuda.synchronize()
+        assert torch.equal(want.view(torch.int16), y.view(torch.int16))
+
+
+def test_ring_runs_back_to_back_and_in_a_graph(nf4):
+    """Two runs enqueued without a host sync reuse the slots safely; a captured run replays to the
+    same bytes, and an eager run after the capture still agrees."""
+    from nf4_weight_only_gb300 import synth
+    n, k = 4096, 4096
+    a = [_host_weights(nf4, 500 + i, n, k) for i in range(3)]
+    b = [_host_weights(nf4, 510 + i, n, k) for i in range(3)]
+    x = synth.device_activations_bf16(520, 1, k, DEV)
+    ya = [torch.empty((1, n), dtype=torch.bfloat16, device=DEV) for _ in a]
+    yb = [torch.empty((1, n), dtype=torch.bfloat16, device=DEV) for _ in b]
+    want = []
+    for cd, sd, _, _ in a + b:
+        w = torch.empty((1, n), dtype=torch.bfloat16, device=DEV)
+        nf4.nf4_linear(x, cd, sd, w)
+        want.append(w)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=DEV)
+    with nf4.Ring(nf4.Ring.bytes_needed(n, k)) as ring:
+        ring.run([(x, m[2], m[3], y) for m, y in zip(a, ya)], stream)
+        ring.run([(x, m[2], m[3], y) for m, y in zip(b, yb)], stream)
+        torch.cuda.synchronize()
+        for w, y in zip(want, ya + yb):
+            assert torch.equal(w.view(torch.int16), y.view(torch.int16))
+        for y in ya + yb:
+            y.zero_()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            ring.run([(x, m[2], m[3], y) for m, y in zip(a + b, ya + yb)], stream)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        for w, y in zip(want, ya + yb):
+            assert torch.equal(w.view(torch.int16), y.view(torch.int16))
+        for y in yb:
+            y.zero_()
+        ring.run([(x, m[2], m[3], y) for m, y in zip(b, yb)], stream)
+        torch.cuda.synchronize()
+        for w, y in zip(want[3:], yb):
+            assert torch.equal(w.view(torch.int16), y.view(torch.int16))
+
+
+def test_ring_errors(nf4):
+    """A matrix larger than a slot and pageable host memory are refused before anything is
+    enqueued; the ring keeps working afterwards."""
+    from nf4_weight_only_gb300 import synth
+    n, k = 1024, 2048
+    cd, sd, ch, sh = _host_weights(nf4, 600, n, k)
+    x = synth.device_activations_bf16(601, 1, k, DEV)
+    y = torch.full((1, n), 7.0, dtype=torch.bfloat16, device=DEV)
+    with nf4.Ring(nf4.Ring.bytes_needed(n, k) - 16) as small:
+        with pytest.raises(nf4.NF4Error) as e:
+            small.run([(x, ch, sh, y)])
+        assert e.value.status == 2
+    with nf4.Ring(nf4.Ring.bytes_needed(n, k)) as ring:
+        with pytest.raises(nf4.NF4Error) as e:
+            ring.run([(x, ch.clone(), sh, y)])  # clone(): pageable host memory
+        assert e.value.status == 7
+        torch.cuda.synchronize()
+        assert torch.all(y == 7.0)
+        ring.run([(x, ch, sh, y)])
+        want = torch.empty_like(y)
+        nf4.nf4_linear(x, cd, sd, want)
+        torch.cuda.synchronize()
+        assert torch.equal(want.view(torch.int16), y.view(torch.int16))
