@@ -33,6 +33,8 @@ namespace nf4 {
 namespace {
 
 constexpr int kMaxWarps = 16;  // consumer warps per CTA (slices x row lanes)
+constexpr int kHalfWarps = 9;  // consumer warps of a CTA that leaves room for a second one
+constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
 constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
 // V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
@@ -289,8 +291,9 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 #pragma unroll
             for (int jj = 0; jj < RMAX; jj++) {
                 const int j = q * L.R + jj;
-                const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * j);
-                rv[jj] = jj < L.R && meta.valid && meta.problem < P.count;  // warp-uniform
+                RowMeta meta = {0, 0, 0, 0};
+                if (jj < L.R) meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * j);  // warp-uniform
+                rv[jj] = meta.valid && meta.problem < P.count;
                 uint32_t sc = 0;
                 if (rv[jj] && active)
                     sc = *reinterpret_cast<const uint16_t*>(stg + L.scales_off + j * L.swin + meta.scale_off + 2 * g);
@@ -307,7 +310,9 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                 float a0[MT], a1[MT];
 #pragma unroll
                 for (int tt = 0; tt < MT; tt++) a0[tt] = a1[tt] = 0.0f;
-                const uint8_t* crow = stg + j * L.row_code_bytes + s * 32 * CB + lane * CB;
+                // A lane past the last group reads its row's first bytes instead (its x is zero), so
+                // that no read leaves the row block.
+                const uint8_t* crow = stg + j * L.row_code_bytes + (active ? s * 32 * CB + lane * CB : 0);
 #pragma unroll
                 for (int c = 0; c < CHUNKS; c++) {
                     const uint4 cw = lds128(crow + 16 * (c ^ sw));
@@ -377,19 +382,44 @@ TableState g_tables;
 
 template <int MT, int LPG, int RMAX>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
-    constexpr int CB = kGroup / LPG / 2;
     constexpr int GPW = 32 / LPG;
     const int64_t N = P.row0[P.count];
     const int G = static_cast<int>(K / kGroup);
     GemvLayout L = {};
     L.S = (G + GPW - 1) / GPW;
-    // Rows per consumer warp: RMAX whenever K spans several slices (a lane then holds one group per
-    // row, and more rows multiply the independent work per block), else 2 for large matrices and 1
-    // when two would leave SMs idle.
-    L.R = L.S > 1 ? RMAX : (N >= static_cast<int64_t>(2) * kMaxWarps * num_sms ? 2 : 1);
-    int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
-    const int qmax = L.S >= kMaxWarps ? 1 : kMaxWarps / L.S;
-    L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
+    // Launch shape (measured on the 3B-shaped decode pass: 144 launches in one graph, chained by
+    // programmatic dependent launch):
+    //  - K over several slices: whole-SM CTAs, RMAX rows per warp, as many row lanes as the rows
+    //    need, the deepest ring that fits;
+    //  - one slice and up to 2 * kMaxWarps rows per SM: row blocks sized for about 1.7 blocks per
+    //    CTA (two rows per warp when a block has at most 8 rows), so that the weights of a CTA's
+    //    second block arrive while its first is computed, and a two-stage ring, which leaves room on
+    //    the SM for a CTA of the next launch;
+    //  - one slice and more rows: two CTAs per SM of kHalfWarps - 1 warps with two rows each and half
+    //    the shared memory; the two CTAs interleave their waits and tails.
+    bool half = false;
+    bool cap_ring = false;    // ring no deeper than the CTA's row blocks
+    int64_t slots = num_sms;  // CTAs resident at once
+    if (L.S > 1) {
+        L.R = RMAX;
+        const int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
+        const int qmax = L.S >= kMaxWarps ? 1 : kMaxWarps / L.S;
+        L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
+    } else if (N <= static_cast<int64_t>(2) * kMaxWarps * num_sms) {
+        cap_ring = true;
+        const int64_t rb = (N * 10 + 17LL * num_sms - 1) / (17LL * num_sms);  // rows per block
+        L.R = (rb <= 8 && RMAX >= 2) ? 2 : 1;
+        const int64_t q = (rb + L.R - 1) / L.R;
+        L.Q = static_cast<int>(q < 1 ? 1 : (q > kMaxWarps ? kMaxWarps : q));
+    } else {
+        half = true;
+        cap_ring = true;
+        slots = 2LL * num_sms;
+        L.R = RMAX < 2 ? RMAX : 2;
+        L.Q = kHalfWarps - 1;
+    }
+    const int64_t nblocks_all = (N + static_cast<int64_t>(L.R) * L.Q - 1) / (static_cast<int64_t>(L.R) * L.Q);
+    const int64_t grid64 = nblocks_all < slots ? nblocks_all : slots;
     L.RB = L.Q * L.R;
     L.row_code_bytes = static_cast<int>(K / 2);
     L.swin = ((2 * G + 15) / 16 + 1) * 16;
@@ -397,13 +427,15 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     L.meta_off = L.scales_off + L.RB * L.swin;
     L.red_off = L.meta_off + 16 * L.RB;
     L.stage_bytes = L.red_off + ((L.S * L.RB * MT * 4 + 15) / 16) * 16;
-    // ring depth: as many stages as fit next to the V table (at most 8, at least 2)
-    const int budget = 227 * 1024 - kVtabBytes - 3 * 8 * 8 - 64;
+    // ring depth: as many stages as fit next to the V table in the CTA's share of shared memory (at
+    // most 8, at least 2; see cap_ring)
+    const int budget = (half ? kHalfSmem : 227 * 1024) - kVtabBytes - 3 * 8 * 8 - 64;
+    const int64_t blocks_per_cta = ((N + L.RB - 1) / L.RB + grid64 - 1) / grid64;
     L.ST = budget / L.stage_bytes;
     if (L.ST > 8) L.ST = 8;
+    if (cap_ring && L.ST > blocks_per_cta) L.ST = static_cast<int>(blocks_per_cta < 2 ? 2 : blocks_per_cta);
     if (L.ST < 2) return cudaErrorInvalidValue;  // a row block does not fit twice
-    const int64_t blocks_needed = (N + L.RB - 1) / L.RB;
-    const int grid = static_cast<int>(blocks_needed < num_sms ? blocks_needed : num_sms);
+    const int grid = static_cast<int>(grid64);
     const size_t smem = kVtabBytes + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
     static std::once_flag attr_once[64];  // the largest possible request, set once per device
     int dev = 0;
