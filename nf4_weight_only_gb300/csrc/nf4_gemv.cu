@@ -33,7 +33,7 @@ namespace nf4 {
 namespace {
 
 constexpr int kMaxWarps = 16;  // consumer warps per CTA (slices x row lanes)
-constexpr int kHalfWarps = 9;  // consumer warps of a CTA that leaves room for a second one
+constexpr int kHalfWarps = 8;  // consumer warps of a CTA that leaves room for a second one
 constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
 constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
@@ -80,11 +80,12 @@ __device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4
     out[3] = prmt(lo, hi, 0x7362u);
 }
 
-// Sum each of V values over the 32 lanes.  Recursive halving: at each of the first log2(V) steps a
-// lane keeps the half of its values selected by one lane bit and adds its partner's copy of that
-// half; the remaining steps are a plain butterfly.  Afterwards lane l holds value l >> (5 - log2 V).
+// First stage of summing each of V values over the 32 lanes.  Recursive halving: at each of log2(V)
+// steps a lane keeps the half of its values selected by one lane bit and adds its partner's copy of
+// that half.  Afterwards lane l holds a partial sum of value l >> (5 - log2 V), and the 32 / V
+// consecutive lanes of a value hold its whole sum between them.
 template <int V>
-__device__ __forceinline__ float reduce_transposed(float (&v)[V], int lane) {
+__device__ __forceinline__ float reduce_halving(float (&v)[V], int lane) {
     int n = V;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
@@ -98,8 +99,6 @@ __device__ __forceinline__ float reduce_transposed(float (&v)[V], int lane) {
                 v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
             }
             n = half;
-        } else {
-            v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], off);
         }
     }
     return v[0];
@@ -146,8 +145,8 @@ struct GemvLayout {
     int ST;              // ring stages
     int row_code_bytes;  // K / 2: one row's codes, copied as they lie in memory
     int swin;            // bytes of one row's scale window (multiple of 16)
-    int stage_bytes;     // RB * (row_code_bytes + swin) + RB * 16 (meta) + red
-    int red_off;         // offset of the [S][RB][MT] partial sums inside a stage
+    int stage_bytes;     // RB * (row_code_bytes + swin) + RB * 16 (meta) + C * 128 (partials)
+    int red_off;         // offset of the [C][32] halved partial sums (one float per consumer lane)
     int meta_off;
     int scales_off;
 };
@@ -157,12 +156,15 @@ struct GemvLayout {
 // fused multiply-adds.  Warp C produces: for each row block it waits until the ring stage is free,
 // copies the block's codes (16-byte chunks, consecutive lanes on consecutive chunks, each chunk
 // placed in the swizzled slot of the consumer lane that owns it), the rows' scale windows and their
-// metadata, and arms the stage's `full` barrier through cp.async.mbarrier.arrive.  With S > 1 the
-// consumers leave per-slice partial sums in the stage and consumer warp 0 adds them in slice order.
+// metadata, and arms the stage's `full` barrier through cp.async.mbarrier.arrive.  After a block
+// each consumer warp halves its per-row sums across lanes once per value bit, leaves one float per
+// lane in the stage and moves on; warp C + 1 (the reducer) adds, for every row of the block, the
+// lanes and slices that hold it in a fixed order, writes y and releases the stage.  The consumers
+// thus never wait on a reduction chain, and the result does not depend on the launch shape.
 // Every wait is bounded; after a timeout the waiting thread records an error code and stops.
 // RMAX bounds the rows a consumer warp takes per block (the launcher picks R <= RMAX).
 template <int MT, int LPG, int RMAX>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+__global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K,
                 const GemvLayout L, uint32_t m1, uint32_t p16) {
     constexpr int WPL = kGroup / LPG;  // weights per consumer lane per row
@@ -188,8 +190,8 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     if (threadIdx.x == 0) {
         for (int st = 0; st < L.ST; st++) {
             mbar_init(bars + 8 * st, 33);  // full: per producer lane after its copies, + lane 0 after the metadata
-            mbar_init(bars + 8 * (L.ST + st), L.S > 1 ? 1 : C);     // empty
-            mbar_init(bars + 8 * (2 * L.ST + st), C);               // part: consumer partials written
+            mbar_init(bars + 8 * (L.ST + st), 1);   // empty: the reducer is done with the stage
+            mbar_init(bars + 8 * (2 * L.ST + st), C);  // part: consumer partials written
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -199,7 +201,41 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     __syncthreads();
     const long long deadline = clock64() + kWaitCycles;
 
-    if (warp == C) {
+    if (warp == C + 1) {
+        // ------------------------------------------------------------------ reducer
+        constexpr int LPV = 32 / V;  // lanes holding one value after the halving steps
+        int st = 0, par = 0;
+        for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, deadline))) {
+                record_error(13);
+                break;
+            }
+            const uint8_t* stg = ring + st * L.stage_bytes;
+            const float* red = reinterpret_cast<const float*>(stg + L.red_off);
+            for (int i = lane; i < L.RB * MT; i += 32) {
+                const int j = i / MT, tt = i - j * MT;
+                const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * j);
+                if (!meta.valid || meta.problem >= P.count) continue;
+                const int q = j / L.R, v = (j - q * L.R) * MT + tt;
+                float acc = 0.0f;
+                for (int ss = 0; ss < L.S; ss++) {
+                    const float4* src = reinterpret_cast<const float4*>(red + (q * L.S + ss) * 32 + v * LPV);
+                    float sub = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < LPV / 4; c++) {
+                        // start rotated by the row (fewer bank conflicts, same order for any launch shape)
+                        const float4 f = src[(c + meta.local_row) & (LPV / 4 - 1)];
+                        sub += (f.x + f.y) + (f.z + f.w);
+                    }
+                    acc += sub;
+                }
+                const int np = P.row0[meta.problem + 1] - P.row0[meta.problem];
+                P.y[meta.problem][static_cast<int64_t>(tt) * np + meta.local_row] = bf16_bits(acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (L.ST + st));
+        }
+    } else if (warp == C) {
         // ------------------------------------------------------------------ producer
         // The producer moves weights only (codes, scales, row metadata into shared memory), which
         // the previous grid in the stream does not write: it starts at once, without the
@@ -208,9 +244,8 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         // Lane j copies rows j, j + 32, ... of the block: each row's codes with one bulk copy
         // (transaction bytes on the stage's `full` barrier) and its scale window with zero-filling
         // 16-byte copies.  Every row of the block gets its metadata (valid = 0 past the end).
-        for (int64_t t = 0; t < my_blocks; t++) {
-            const int st = static_cast<int>(t % L.ST);
-            const int round = static_cast<int>(t / L.ST);
+        int st = 0, round = 0;  // ring stage of block t and how often the ring has wrapped
+        for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, round += st == 0) {
             if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (L.ST + st), (round - 1) & 1, deadline))) {
                 record_error(11);
                 break;
@@ -272,13 +307,16 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                 xr[tt][4 * i + 3] = v.w;
             }
         }
-        for (int64_t t = 0; t < my_blocks; t++) {
-            const int st = static_cast<int>(t % L.ST);
-            const int par = static_cast<int>(t / L.ST) & 1;
+        int st = 0, par = 0;  // ring stage of block t and the phase parity of its barriers
+        for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, deadline))) {
                 record_error(12);
                 break;
             }
+            // With several blocks per CTA, the upper half of the consumer warps starts about half a
+            // block later: the warps of a CTA then no longer reach their latency-bound steps
+            // (prologue loads, reduction, write-back) together, and the SM keeps issuing lookups.
+            if (t == 0 && my_blocks >= 3 && ((warp >> 2) & 1)) __nanosleep(400u * L.R);
             const uint8_t* stg = ring + st * L.stage_bytes;
             float part[V];
 #pragma unroll
@@ -332,44 +370,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 #pragma unroll
                 for (int tt = 0; tt < MT; tt++) part[jj * MT + tt] = (a0[tt] + a1[tt]) * pow2[jj];
             }
-            const float total = reduce_transposed<V>(part, lane);
-            constexpr int lanes_per_value = 32 / V;
-            const int idx = lane / lanes_per_value;
-            const bool writer = (lane % lanes_per_value) == 0 && idx < L.R * MT;
-            const int jj = idx / MT, tt = idx % MT;
-            if (L.S == 1) {
-                if (writer) {
-                    const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * (q * L.R + jj));
-                    if (meta.valid && meta.problem < P.count) {
-                        const int np = P.row0[meta.problem + 1] - P.row0[meta.problem];
-                        P.y[meta.problem][static_cast<int64_t>(tt) * np + meta.local_row] = bf16_bits(total);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + 8 * (L.ST + st));
-            } else {
-                float* red = reinterpret_cast<float*>(ring + st * L.stage_bytes + L.red_off);
-                if (writer) red[(s * L.RB + q * L.R + jj) * MT + tt] = total;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + 8 * (2 * L.ST + st));
-                if (warp == 0) {  // add the slices in order and release the stage
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, deadline))) {
-                        record_error(13);
-                        break;
-                    }
-                    for (int i = lane; i < L.RB * MT; i += 32) {
-                        const RowMeta meta = *reinterpret_cast<const RowMeta*>(stg + L.meta_off + 16 * (i / MT));
-                        float acc = 0.0f;
-                        for (int ss = 0; ss < L.S; ss++) acc += red[ss * L.RB * MT + i];
-                        if (meta.valid && meta.problem < P.count) {
-                            const int np = P.row0[meta.problem + 1] - P.row0[meta.problem];
-                            P.y[meta.problem][static_cast<int64_t>(i % MT) * np + meta.local_row] = bf16_bits(acc);
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars + 8 * (L.ST + st));
-                }
-            }
+            // leave this warp's halved sums in the stage for the reducer
+            float* red = reinterpret_cast<float*>(ring + st * L.stage_bytes + L.red_off);
+            red[warp * 32 + lane] = reduce_halving<V>(part, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (2 * L.ST + st));
         }
     }
 }
@@ -395,7 +400,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     //    CTA (two rows per warp when a block has at most 8 rows), so that the weights of a CTA's
     //    second block arrive while its first is computed, and a two-stage ring, which leaves room on
     //    the SM for a CTA of the next launch;
-    //  - one slice and more rows: two CTAs per SM of kHalfWarps - 1 warps with two rows each and half
+    //  - one slice and more rows: two CTAs per SM of kHalfWarps warps with two rows each and half
     //    the shared memory; the two CTAs interleave their waits and tails.
     bool half = false;
     bool cap_ring = false;    // ring no deeper than the CTA's row blocks
@@ -416,7 +421,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
         cap_ring = true;
         slots = 2LL * num_sms;
         L.R = RMAX < 2 ? RMAX : 2;
-        L.Q = kHalfWarps - 1;
+        L.Q = kHalfWarps;
     }
     const int64_t nblocks_all = (N + static_cast<int64_t>(L.R) * L.Q - 1) / (static_cast<int64_t>(L.R) * L.Q);
     const int64_t grid64 = nblocks_all < slots ? nblocks_all : slots;
@@ -426,7 +431,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     L.scales_off = L.RB * L.row_code_bytes;
     L.meta_off = L.scales_off + L.RB * L.swin;
     L.red_off = L.meta_off + 16 * L.RB;
-    L.stage_bytes = L.red_off + ((L.S * L.RB * MT * 4 + 15) / 16) * 16;
+    L.stage_bytes = L.red_off + L.S * L.Q * 32 * 4;  // one float per consumer lane
     // ring depth: as many stages as fit next to the V table in the CTA's share of shared memory (at
     // most 8, at least 2; see cap_ring)
     const int budget = (half ? kHalfSmem : 227 * 1024) - kVtabBytes - 3 * 8 * 8 - 64;
@@ -448,7 +453,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(32 * (L.S * L.Q + 1));
+    cfg.blockDim = dim3(32 * (L.S * L.Q + 2));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
