@@ -189,6 +189,41 @@ nf4_status nf4_ring_run(nf4_ring* ring, const nf4_host_linear* ops, int64_t coun
 nf4_status nf4_ring_destroy(nf4_ring* ring);
 
 /*
+ * nf4_linear_host_noalloc - one linear whose packed weights live in page-locked host memory, staged
+ * through a device buffer that is part of the library itself, so that nothing is allocated.  The
+ * pages have no counterpart: it is an addition of this library.
+ *
+ * Who needs it: a caller that cannot allocate device memory when it runs the layer.  Examples: a
+ * host application whose own pool allocator has already reserved the GPU's memory (a cudaMalloc
+ * from the library would fail or fragment that pool), or a decode loop that cannot afford
+ * cudaMalloc / cudaFree, which may synchronise the whole device.  nf4_ring_create allocates its
+ * slots with cudaMalloc; this call uses one static device array of NF4_NOALLOC_SLOT_BYTES instead.
+ * Every device on which the library runs holds that array until the process exits.
+ *
+ *   x       in   device, bf16 bits [M][K]
+ *   codes   in   page-locked host, uint8 [N][K/2]
+ *   scales  in   page-locked host, fp16 bits [N][K/64]
+ *   y       out  device, bf16 bits [M][N]; must not overlap x
+ *
+ * On `stream` the call copies codes and scales into the array and then runs nf4_linear on that copy;
+ * y is bit for bit what nf4_linear gives on device-resident weights.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ * Limit: N*K/2 rounded up to 256, plus N*(K/64)*2, must not exceed NF4_NOALLOC_SLOT_BYTES (16 MiB,
+ * e.g. 11008 x 2048 fits); a larger linear returns NF4_ERR_SHAPE and nothing is enqueued.  Host
+ * buffers that are not page-locked give NF4_ERR_MEMORY.  Other errors as for nf4_linear.  The host
+ * buffers must stay unchanged until the call's work on `stream` has finished.
+ * Sharing: all calls on a device use the same array, which keeps the weights of the last call (each
+ * call rewrites every byte the kernels read, so nothing needs clearing).  Calls on one stream are
+ * ordered and safe; calls whose work may overlap on the GPU (different streams with no ordering
+ * between them) race on the array and give wrong results.
+ * Set-up: the first call on a device looks up the array's device address (and, like the first
+ * nf4_linear, builds the kernels' lookup table); make that first call before any stream capture.
+ */
+#define NF4_NOALLOC_SLOT_BYTES (16 * 1024 * 1024)
+nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * nf4_check_device_error - diagnostics: read and clear the device-side error words of the current
  * device.  The linear kernels bound every pipeline wait (about one second); a wait that runs out
  * records a nonzero code (1..39), and the kernel drains and exits instead of hanging.  nf4_embed

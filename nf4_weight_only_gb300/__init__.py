@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_
 
 # Every symbol include/nf4.h declares.
 EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_embed",
-            "nf4_ring_create", "nf4_ring_run", "nf4_ring_destroy",
+            "nf4_ring_create", "nf4_ring_run", "nf4_ring_destroy", "nf4_linear_host_noalloc",
             "nf4_check_device_error", "nf4_status_str", "nf4_abi_version")
 
 
@@ -69,6 +69,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_ring_run.restype = ci
     lib.nf4_ring_destroy.argtypes = [vp]
     lib.nf4_ring_destroy.restype = ci
+    lib.nf4_linear_host_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.nf4_linear_host_noalloc.restype = ci
     lib.nf4_status_str.argtypes = [ci]
     lib.nf4_status_str.restype = ctypes.c_char_p
     lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -196,6 +198,19 @@ class Ring:
 
     def __exit__(self, *exc):
         self.close()
+
+
+NOALLOC_SLOT_BYTES = 16 * 1024 * 1024  # NF4_NOALLOC_SLOT_BYTES
+
+
+def nf4_linear_host_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
+                            stream=None) -> None:
+    """y[M, N] = x[M, K] * w_hat^T with codes [N, K/2] and scales [N, K/64] in pinned host memory,
+    staged through the library's static device buffer (no allocation; at most NOALLOC_SLOT_BYTES)."""
+    m, k = x.shape
+    n = codes.shape[0]
+    _check(load().nf4_linear_host_noalloc(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
+           "nf4_linear_host_noalloc")
 
 
 def nf4_check_device_error() -> int:

@@ -207,3 +207,54 @@ nf4_status nf4_ring_destroy(nf4_ring* r) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// One streamed linear without any allocation: the weights pass through a device array that is part
+// of the library image instead of a slot from cudaMalloc.  The array's device address is looked up
+// once per device (cudaGetSymbolAddress in host code gives the address for the current device; the
+// name alone is a host-side stand-in that no kernel may be given).
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_slot[NF4_NOALLOC_SLOT_BYTES];
+
+constexpr int kMaxSlotDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[kMaxSlotDevices] = {};
+
+// Device address of g_noalloc_slot on `device` (the current device); nullptr on failure.
+uint8_t* noalloc_slot(int device) {
+    if (device < 0 || device >= kMaxSlotDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_slot) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[device] = static_cast<uint8_t*>(p);
+    }
+    return g_noalloc_ptr[device];
+}
+
+}  // namespace
+
+extern "C" nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales,
+                                              uint16_t* y, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    const nf4_host_linear op = {x, codes, scales, y, M, N, K};
+    nf4_status st = check_op(op, NF4_NOALLOC_SLOT_BYTES);
+    if (st != NF4_OK || M == 0 || N == 0) return st;
+    int dev = 0, sms = 0;
+    if ((st = static_cast<nf4_status>(nf4::abi_current_device(&dev, &sms))) != NF4_OK) return st;
+    uint8_t* slot = noalloc_slot(dev);
+    if (!slot) return NF4_ERR_CUDA;
+    uint16_t* slot_scales = reinterpret_cast<uint16_t*>(slot + scales_offset(op));
+    if (cudaMemcpyAsync(slot, codes, static_cast<size_t>(codes_bytes(op)), cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(slot_scales, scales, static_cast<size_t>(scales_bytes(op)), cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return NF4_ERR_CUDA;
+    }
+    return nf4_linear(x, slot, slot_scales, y, M, N, K, stream);
+}
