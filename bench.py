@@ -155,6 +155,7 @@ def run_ours(args, rank, world):
     ys = [{name: torch.empty((1, lin.n), dtype=torch.bfloat16, device=dev) for name, (lin, _, _) in m.items()}
           for m in layers]
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()  # x is drawn on the default stream
 
     def step():
         for mats, yl in zip(layers, ys):
@@ -355,6 +356,7 @@ def prefill_bench(nf4, synth, dev, pk):
     for m in wl.tokens:
         xs = {k: synth.device_activations_bf16(99 + k, m, k, dev) for k in {l.k for l in wl.linears}}
         ys = {name: torch.empty((m, lin.n), dtype=torch.bfloat16, device=dev) for name, (lin, _, _) in mats.items()}
+        torch.cuda.synchronize()  # weights and x are made on the default stream
 
         def step():
             for names in groups:

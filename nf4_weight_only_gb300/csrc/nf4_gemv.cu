@@ -545,7 +545,7 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(P.cta0[P.count]), static_cast<unsigned>((M + T - 1) / T));
-    cfg.blockDim = dim3(st::kThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

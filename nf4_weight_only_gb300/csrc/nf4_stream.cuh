@@ -27,10 +27,12 @@
 // codes ring is released by the dequant warps, the x ring by the MMAs, and the tensor-memory ring of
 // A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
 //
-// Warp roles (352 threads): warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp
-// copies scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2-9 are two sets of
-// four dequant warps (a set takes every other stage; the four warps of a set cover the four 32-lane
-// quarters of tensor memory) that also run the epilogue of every other tile, warp 10 streams x.
+// Warp roles: warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp copies
+// scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2 .. 4*S+1 are S sets of
+// four dequant warps (a set takes every S-th stage; the four warps of a set cover the four 32-lane
+// quarters of tensor memory) that also run the epilogue of every S-th tile, and the last warp
+// streams x.  S = 4 for the wide tiles (608 threads) and 3 for T <= 32 (480 threads): with fewer
+// sets the lookups' dependent integer chains leave the dequant warps latency-bound.
 // Weights do not depend on the previous kernel in the stream, so warp 0 never waits for it; only x
 // and y do.  Each producer runs as far ahead as its own ring allows.
 //
@@ -43,12 +45,16 @@
 
 #include <cuda.h>
 
+#ifndef KSETS_WIDE
+#define KSETS_WIDE 4
+#endif
+#ifndef KSETS_NARROW
+#define KSETS_NARROW 3
+#endif
+
 namespace nf4 {
 namespace st {
 
-constexpr int kSets = 2;                        // dequant warp sets
-constexpr int kXWarp = 2 + 4 * kSets;           // the x producer, after the dequant warps
-constexpr int kThreads = 32 * (kXWarp + 1);     // 352
 constexpr uint32_t kScaleSlot = 6144;           // R * (S + 2) 16-byte chunks with R * S <= 128
 constexpr uint32_t kLoadBytes = 16384;          // one codes load stage: <= 128 MMA rows x 128 bytes
 constexpr int kMaxProblems = 8;
@@ -64,6 +70,11 @@ template <int T>
 struct Cfg {
     static constexpr bool kWide = T >= 64;
     static constexpr int kAccN = kWide ? 1 : kAcc;                    // accumulators
+    // dequant warp sets (four warps each, one per 32-lane quarter of tensor memory); a set takes
+    // every kSets-th stage, so more sets hide more of the lookups' latency
+    static constexpr int kSets = kWide ? KSETS_WIDE : KSETS_NARROW;
+    static constexpr int kXWarp = 2 + 4 * kSets;      // the x producer, after the dequant warps
+    static constexpr int kThreads = 32 * (kXWarp + 1);
     static constexpr int kTmemCols = 512;
     static constexpr int kJMax = kWide ? T : (T == 1 ? 16 : (T <= 4 ? 32 : 64));  // columns of B and of each D
     static constexpr int kSMax = kWide ? 1 : (kJMax / T < 8 ? kJMax / T : 8);      // K-slices per tile
@@ -81,7 +92,10 @@ struct Cfg {
     static constexpr uint32_t kOffScales = kOffVtab + 32768;
     static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
     static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
-    static constexpr uint32_t kBytes = kOffBars + 512;
+    static constexpr uint32_t kBytes = kOffBars + 1024;
+    static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
+    static_assert(8 * (2 * (kLoadStages + kXStages + kAStages + kScaleStages) + 2 * kSets + 2) + 4 <= 1024,
+                  "barrier area");
 };
 
 // k-stages per codes load stage for a tile of S slices: 128 bytes a row for S = 1, 2, 4.
@@ -230,7 +244,7 @@ __device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, long l
 }
 
 template <int T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     stream_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
                   const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
     using C = Cfg<T>;
@@ -252,11 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile read (8 dequant warps)
     // accumulators complete (commit), one barrier per epilogue set: a set waits only for its own
     // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
-    const uint32_t b_dfull = b_sempty + 8 * NSS;        // [2]
-    const uint32_t b_dfree = b_dfull + 16;              // accumulators read (4 warps)
-    const uint32_t b_ep = b_dfree + 8;                  // [2] per-set epilogue rendezvous
-    const uint32_t b_mdone = b_ep + 16;                 // every MMA issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + 6));
+    const uint32_t b_dfull = b_sempty + 8 * NSS;        // [kSets]
+    const uint32_t b_dfree = b_dfull + 8 * C::kSets;    // accumulators read (4 warps)
+    const uint32_t b_ep = b_dfree + 8;                  // [kSets] per-set epilogue rendezvous
+    const uint32_t b_mdone = b_ep + 8 * C::kSets;       // every MMA issued has completed
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + 2 * C::kSets + 2));
 
     // this CTA's problem and rows
     int p = 0;
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NL; i++) {
             mbar_init(b_lfull + 8 * i, 1);
-            mbar_init(b_lempty + 8 * i, 4 * kSets);
+            mbar_init(b_lempty + 8 * i, 4 * C::kSets);
         }
         for (int i = 0; i < NX; i++) {
             mbar_init(b_xfull + 8 * i, 1);
@@ -283,13 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < NSS; i++) {
             mbar_init(b_sfull + 8 * i, 32);
-            mbar_init(b_sempty + 8 * i, 4 * kSets);
+            mbar_init(b_sempty + 8 * i, 4 * C::kSets);
         }
-        mbar_init(b_dfull, 1);
-        mbar_init(b_dfull + 8, 1);
+        for (int i = 0; i < C::kSets; i++) {
+            mbar_init(b_dfull + 8 * i, 1);
+            mbar_init(b_ep + 8 * i, 4);
+        }
         mbar_init(b_dfree, 4);
-        mbar_init(b_ep, 4);
-        mbar_init(b_ep + 8, 4);
         mbar_init(b_mdone, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -299,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < 2048; i += kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
+    for (int i = threadIdx.x; i < 2048; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
     cp_async_commit();
     cp_async_wait<0>();
     tc_fence_before();
@@ -379,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long dl = clock64() + kDrainCycles;
             for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, dl);
         }
-    } else if (warp == kXWarp) {
+    } else if (warp == C::kXWarp) {
         // ---------------------------------------------------------------- x producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
@@ -460,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aph ^= 1;
                     }
                 }
-                if (ok) mma_commit(b_dfull + 8 * (j & (kSets - 1)));
+                if (ok) mma_commit(b_dfull + 8 * (j % C::kSets));
             }
             mma_commit(b_mdone);  // the CTA exits only after every MMA it issued has completed
             mbar_wait(b_mdone, 0, clock64() + kDrainCycles);
@@ -499,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int h = kb & 1;  // sub-stage: A columns 32h .. 32h + 31 of the stage's slot
-                if ((q & (kSets - 1)) == set) {
+                if (q % C::kSets == set) {
                     if (h == 0 && around > 0 && !warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline)) {
                         record_error(27);
                         ok = false;
@@ -585,9 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok || j % kSets != set) continue;
+            if (!ok || j % C::kSets != set) continue;
             // ------------------------------------------------------------ epilogue of tile j
-            if (!warp_wait(b_dfull + 8 * set, (j / kSets) & 1, deadline)) {
+            if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, deadline)) {
                 record_error(26);
                 ok = false;
                 break;
