@@ -257,13 +257,13 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
 
     // barriers
     const uint32_t b_lfull = sbase + C::kOffBars;       // [NL] codes load stage landed (tx)
-    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage read (8 dequant warps)
+    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage seen and read (every dequant warp)
     const uint32_t b_xfull = b_lempty + 8 * NL;         // [NX] x tile landed (tx)
     const uint32_t b_xempty = b_xfull + 8 * NX;         // [NX] x tile read by the MMAs (commit)
     const uint32_t b_afull = b_xempty + 8 * NX;         // [NA] A tile in tensor memory (4 warps)
     const uint32_t b_aempty = b_afull + 8 * NA;         // [NA] A tile read by the MMAs (commit)
     const uint32_t b_sfull = b_aempty + 8 * NA;         // [NSS] scale tile landed (32 producer lanes)
-    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile read (8 dequant warps)
+    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile seen and read (every dequant warp)
     // accumulators complete (commit), one barrier per epilogue set: a set waits only for its own
     // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
     const uint32_t b_dfull = b_sempty + 8 * NSS;        // [kSets]
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NL; i++) {
             mbar_init(b_lfull + 8 * i, 1);
-            mbar_init(b_lempty + 8 * i, 4 * C::kSets);
+            mbar_init(b_lempty + 8 * i, 4 * C::kSets);  // every dequant warp releases every load stage
         }
         for (int i = 0; i < NX; i++) {
             mbar_init(b_xfull + 8 * i, 1);
@@ -488,11 +488,46 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint4* vtab = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
         bool ok = true;
-        int q = 0, aslot = 0, around = 0, lslot = 0, sslot = 0, ep_uses = 0;
-        uint32_t lph = 0, sph = 0;
+        int ep_uses = 0;
+        // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
+        // ring slots and phases follow from them, so a set visits only its own stages.
+        int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
+        // A parity wait names one of two phases, so it is sound only while the barrier is neither a
+        // phase behind (this warp saw the previous fill of the slot) nor a phase ahead (the producer
+        // refilled the slot before this warp saw it).  Hence every warp sees every codes load stage
+        // and scale tile in the producer's own order (by sub-stage: the load stage, then the scale
+        // tile), and releases each exactly once: at the end of its last stage that reads it, or at
+        // once if its set reads none of it.  A warp never waits while holding a slot the producer
+        // needs first, so the rings cannot deadlock.
+        int kobs = 0;  // next sub-stage of tile j whose load stage / scale tile this warp has to see
+        int U = 1;
+        auto see = [&](int kend, int lkeep, int skeep) {  // see sub-stages kobs .. kend; release
+            bool good = true;                              // load stages < lkeep, scale tiles < skeep
+            for (; good && kobs <= kend; kobs++) {
+                if ((kobs & (U - 1)) == 0) {
+                    const int L = l0 + kobs / U;
+                    good = warp_wait(b_lfull + 8 * (L % NL), (L / NL) & 1, deadline);
+                    if (good && kobs / U < lkeep && lane == 0) mbar_arrive(b_lempty + 8 * (L % NL));
+                }
+                if (good && (kobs & 7) == 0) {
+                    const int S = s0 + kobs / 8;
+                    good = warp_wait(b_sfull + 8 * (S % NSS), (S / NSS) & 1, deadline);
+                    if (good && kobs / 8 < skeep && lane == 0) mbar_arrive(b_sempty + 8 * (S % NSS));
+                }
+            }
+            return good;
+        };
         for (int j = 0; j < ntiles && ok; j++) {
+            q0 += nst_prev;
+            l0 += nload_prev;
+            s0 += nscale_prev;
             const Tile t = tile_of(P, rbeg, rows_cta, j);
-            const int U = load_span(t.s);
+            U = load_span(t.s);
+            kobs = 0;
+            const int nst = t.nt / 2, nload = (t.nt + U - 1) / U, nscale = (t.nt + 7) / 8;
+            nst_prev = nst;
+            nload_prev = nload;
+            nscale_prev = nscale;
             const int r = i / t.s, sl = i - (i / t.s) * t.s;
             const bool lane_ok = r < t.rows;
             const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
@@ -501,104 +536,96 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const uint32_t rowb = 32u * U * t.s;
             const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
             // this lane's scale inside a scale tile: row r's window starts at the 16-byte boundary
-            // below its first scale; stage kb adds 2 * (kb mod 8) * S bytes
+            // below its first scale; sub-stage kb adds 2 * (kb mod 8) * S bytes
             const uint32_t soff = r * (t.s + 2) * 16 +
                                   static_cast<uint32_t>((static_cast<int64_t>(t.row0 + r) * G * 2) & 15) + 2 * sl;
-            for (int kb = 0; kb < t.nt && ok; kb++) {
-                const int u = kb & (U - 1);
-                // every warp waits for every load stage and scale tile it passes, in order
-                if ((u == 0 && !warp_wait(b_lfull + 8 * lslot, lph, deadline)) ||
-                    ((kb & 7) == 0 && !warp_wait(b_sfull + 8 * sslot, sph, deadline))) {
+            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets)
+            for (int kb2 = (set - q0 % C::kSets + C::kSets) % C::kSets; kb2 < nst && ok; kb2 += C::kSets) {
+                const int gq = q0 + kb2;
+                const int aslot = gq % NA, around = gq / NA;
+                const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
+                const int lfirst = kbs / U, llast = (kbs + 1) / U;  // its codes load stage(s), tile-relative
+                const int si = kbs / 8;                   // its scale tile, tile-relative
+                const int sslot = (s0 + si) % NSS;
+                bool good = see(kbs + 1, lfirst, si);
+                if (good && around > 0) good = warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline);
+                if (!good) {
                     record_error(26);
                     ok = false;
                     break;
                 }
-                const int h = kb & 1;  // sub-stage: A columns 32h .. 32h + 31 of the stage's slot
-                if (q % C::kSets == set) {
-                    if (h == 0 && around > 0 && !warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline)) {
-                        record_error(27);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (warp_ok) {
-                        uint32_t out[32];
-                        const int g = kb * t.s + sl;
-                        if (lane_ok && g < G) {
-                            const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + r * rowb;
-                            const uint32_t ch = static_cast<uint32_t>((u * t.s + sl) * 2);
-                            const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
-                            const uint16_t sc = *reinterpret_cast<const uint16_t*>(
-                                smem + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s);
-                            // scale = sign * 2^E * (1 + m/1024); w_hat = 2^E * V[m][c]: the table row
-                            // gives V, E is added to the exponent field of every entry.  An odd E flips
-                            // the exponent's low bit (bit 7 of the low byte) and carries into the high
-                            // byte; E >> 1 is added to the high byte (exponent >> 1), byte by byte.
-                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
-                            const uint32_t m = (sb >> 13) & 0x3FFu;
-                            const int e = static_cast<int>((sb >> 23) & 0xFFu) - 127;
-                            const uint32_t pm = (e & 1) ? 0x80808080u : 0u;
-                            const uint32_t add = static_cast<uint32_t>(e >> 1) * 0x01010101u;
-                            const uint32_t sgn = (sb >> 31) ? 0x80808080u : 0u;
-                            uint4 tl = vtab[m + (m & ~7u)];
-                            uint4 th = vtab[m + (m & ~7u) + 8];
-                            th.x = (th.x + add + ((tl.x & pm) >> 7)) ^ sgn;
-                            th.y = ((th.y + add + ((tl.y & pm) >> 7)) & 0x00FFFFFFu) ^ sgn;  // code 7 stays 0
-                            th.z = (th.z + add + ((tl.z & pm) >> 7)) ^ sgn;
-                            th.w = (th.w + add + ((tl.w & pm) >> 7)) ^ sgn;
-                            tl.x ^= pm;
-                            tl.y = (tl.y ^ pm) & 0x00FFFFFFu;
-                            tl.z ^= pm;
-                            tl.w ^= pm;
-                            if ((sb & 0x7FFFFFFFu) == 0u) {  // zero scale
-                                tl = make_uint4(0, 0, 0, 0);
-                                th = make_uint4(0, 0, 0, 0);
-                            }
-                            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                            for (int w = 0; w < 8; w++) {
-                                uint32_t o4[4];
-                                lookup8(words[w], tl, th, P.m1, P.p16, o4);
-                                out[4 * w + 0] = o4[0];
-                                out[4 * w + 1] = o4[1];
-                                out[4 * w + 2] = o4[2];
-                                out[4 * w + 3] = o4[3];
-                            }
-                        } else {
-#pragma unroll
-                            for (int w = 0; w < 32; w++) out[w] = 0u;
+                tc_fence_after();
+#pragma unroll 1
+                for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
+                    if (!warp_ok) break;
+                    const int kb = kbs + h;
+                    const int u = kb & (U - 1);
+                    const int lslot = (l0 + kb / U) % NL;
+                    uint32_t out[32];
+                    const int g = kb * t.s + sl;
+                    if (lane_ok && g < G) {
+                        const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + r * rowb;
+                        const uint32_t ch = static_cast<uint32_t>((u * t.s + sl) * 2);
+                        const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
+                        const uint16_t sc = *reinterpret_cast<const uint16_t*>(
+                            smem + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s);
+                        // scale = sign * 2^E * (1 + m/1024); w_hat = 2^E * V[m][c]: the table row
+                        // gives V, E is added to the exponent field of every entry.  An odd E flips
+                        // the exponent's low bit (bit 7 of the low byte) and carries into the high
+                        // byte; E >> 1 is added to the high byte (exponent >> 1), byte by byte.
+                        const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
+                        const uint32_t m = (sb >> 13) & 0x3FFu;
+                        const int e = static_cast<int>((sb >> 23) & 0xFFu) - 127;
+                        const uint32_t pm = (e & 1) ? 0x80808080u : 0u;
+                        const uint32_t add = static_cast<uint32_t>(e >> 1) * 0x01010101u;
+                        const uint32_t sgn = (sb >> 31) ? 0x80808080u : 0u;
+                        uint4 tl = vtab[m + (m & ~7u)];
+                        uint4 th = vtab[m + (m & ~7u) + 8];
+                        th.x = (th.x + add + ((tl.x & pm) >> 7)) ^ sgn;
+                        th.y = ((th.y + add + ((tl.y & pm) >> 7)) & 0x00FFFFFFu) ^ sgn;  // code 7 stays 0
+                        th.z = (th.z + add + ((tl.z & pm) >> 7)) ^ sgn;
+                        th.w = (th.w + add + ((tl.w & pm) >> 7)) ^ sgn;
+                        tl.x ^= pm;
+                        tl.y = (tl.y ^ pm) & 0x00FFFFFFu;
+                        tl.z ^= pm;
+                        tl.w ^= pm;
+                        if ((sb & 0x7FFFFFFFu) == 0u) {  // zero scale
+                            tl = make_uint4(0, 0, 0, 0);
+                            th = make_uint4(0, 0, 0, 0);
                         }
-                        tmem_st32(tmem_base + lane_addr + C::kDCols + 64 * aslot + 32 * h, out);
+                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int w = 0; w < 8; w++) {
+                            uint32_t o4[4];
+                            lookup8(words[w], tl, th, P.m1, P.p16, o4);
+                            out[4 * w + 0] = o4[0];
+                            out[4 * w + 1] = o4[1];
+                            out[4 * w + 2] = o4[2];
+                            out[4 * w + 3] = o4[3];
+                        }
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < 32; w++) out[w] = 0u;
                     }
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(b_afull + 8 * aslot);
-                    }
+                    tmem_st32(tmem_base + lane_addr + C::kDCols + 64 * aslot + 32 * h, out);
                 }
-                if (u == U - 1 || kb == t.nt - 1) {  // leaving a load stage
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_lempty + 8 * lslot);
-                    if (++lslot == NL) {
-                        lslot = 0;
-                        lph ^= 1;
-                    }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b_afull + 8 * aslot);
+                    // a set never reads a load stage in two of its stages (kSets >= 2), so the stage's
+                    // load stages go back now; its scale tile (4 stages) only after the set's last
+                    // stage in it
+                    for (int li = lfirst; li <= llast; li++) mbar_arrive(b_lempty + 8 * ((l0 + li) % NL));
+                    const int nxt = kb2 + C::kSets;
+                    if (nxt >= nst || (2 * nxt) / 8 != si) mbar_arrive(b_sempty + 8 * sslot);
                 }
-                if ((kb & 7) == 7 || kb == t.nt - 1) {  // leaving a scale tile
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_sempty + 8 * sslot);
-                    if (++sslot == NSS) {
-                        sslot = 0;
-                        sph ^= 1;
-                    }
-                }
-                if (h == 1) {
-                    q++;
-                    if (++aslot == NA) {
-                        aslot = 0;
-                        around++;
-                    }
-                }
+            }
+            // see and release the rest of tile j, so that no warp holds a slot that the other sets
+            // still need while it waits for the accumulators or moves on to the next tile
+            if (ok && !see(t.nt - 1, nload, nscale)) {
+                record_error(26);
+                ok = false;
             }
             if (!ok || j % C::kSets != set) continue;
             // ------------------------------------------------------------ epilogue of tile j

@@ -344,7 +344,7 @@ def test_linear_grouped(nf4, o, m):
 # K-slices, ragged last stages, every token-tile size
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("m", [5, 8, 16, 32])
-@pytest.mark.parametrize("n,k", [(2048, 11008), (22016, 2048), (19457, 640), (3, 27648)])
+@pytest.mark.parametrize("n,k", [(2048, 11008), (22016, 2048), (19457, 640), (3, 27648), (19500, 320)])
 def test_linear_stream_tiles(nf4, o, m, n, k):
     check_linear(nf4, o, m, n, k, seed=7 * n + k + m)
     assert device_error(nf4) == 0
