@@ -21,7 +21,8 @@
 // per group) and keeps that slice of x in registers as bf16 pairs; it streams four rows at a time
 // (128-bit loads), reduces the four row partial sums across lanes with a transposed butterfly and
 // hands them to the CTA, whose warps cover all slices of the same rows; slice sums are added in a
-// fixed order, so results are deterministic.  The grid is persistent over row blocks.
+// fixed order, so results are deterministic.  The grid is persistent: each CTA owns a contiguous
+// range of rows (the rows split as evenly as the grid allows) and walks it in row blocks.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -183,8 +184,10 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     const uint4* vtab = reinterpret_cast<const uint4*>(smem);
     uint8_t* ring = smem + kVtabBytes;
     const uint32_t bars = sbase + kVtabBytes + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
-    const int64_t nblocks = (static_cast<int64_t>(N) + L.RB - 1) / L.RB;
-    const int64_t my_blocks = blockIdx.x < nblocks ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    // this CTA's rows: a contiguous range, the N rows split as evenly as the grid allows
+    const int64_t rbeg = static_cast<int64_t>(N) * blockIdx.x / gridDim.x;
+    const int64_t rend = static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x;
+    const int64_t my_blocks = (rend - rbeg + L.RB - 1) / L.RB;
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -195,9 +198,6 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < kVtabBytes / 16; i += blockDim.x) cp_async16(smem + 16 * i, &g_vtab[i]);
-    cp_async_commit();
-    cp_async_wait<0>();
     __syncthreads();
     const long long deadline = clock64() + kWaitCycles;
 
@@ -251,14 +251,14 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 break;
             }
             uint8_t* stg = ring + st * L.stage_bytes;
-            const int64_t r0 = (blockIdx.x + t * gridDim.x) * static_cast<int64_t>(L.RB);
-            const int64_t valid_rows = N - r0 < L.RB ? N - r0 : L.RB;
+            const int64_t r0 = rbeg + t * L.RB;
+            const int64_t valid_rows = rend - r0 < L.RB ? rend - r0 : L.RB;
             if (lane == 0) mbar_expect_tx_only(bars + 8 * st, static_cast<uint32_t>(valid_rows * (K / 2)));
             __syncwarp();
             for (int j = lane; j < L.RB; j += 32) {
                 const int64_t r = r0 + j;
                 RowMeta meta = {0, 0, 0, 0};
-                if (r < N) {
+                if (r < rend) {
                     const int pp = problem_of(P, r);
                     const int64_t lr = r - P.row0[pp];
                     bulk_copy_g2s(sbase + static_cast<uint32_t>(kVtabBytes + st * L.stage_bytes + j * L.row_code_bytes),
@@ -292,6 +292,10 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         // Lanes whose bit 2 is set read the two 16-byte halves of their 32 code bytes in the other
         // order (no bank conflicts for eight lanes 32 bytes apart); x is loaded in the same order.
         const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
+        // The V table is for the consumers alone: they copy it while the producer already streams
+        // the first row blocks, and meet on a named barrier before the first lookup.
+        for (int i = threadIdx.x; i < kVtabBytes / 16; i += 32 * C) cp_async16(smem + 16 * i, &g_vtab[i]);
+        cp_async_commit();
         pdl_wait();
         uint32_t xr[MT][WPL / 2];
 #pragma unroll
@@ -307,6 +311,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 xr[tt][4 * i + 3] = v.w;
             }
         }
+        cp_async_wait<0>();
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * C) : "memory");  // every consumer's table chunks landed
         int st = 0, par = 0;  // ring stage of block t and the phase parity of its barriers
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, deadline))) {
@@ -435,7 +441,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     // ring depth: as many stages as fit next to the V table in the CTA's share of shared memory (at
     // most 8, at least 2; see cap_ring)
     const int budget = (half ? kHalfSmem : 227 * 1024) - kVtabBytes - 3 * 8 * 8 - 64;
-    const int64_t blocks_per_cta = ((N + L.RB - 1) / L.RB + grid64 - 1) / grid64;
+    const int64_t blocks_per_cta = ((N + grid64 - 1) / grid64 + L.RB - 1) / L.RB;  // of the largest row range
     L.ST = budget / L.stage_bytes;
     if (L.ST > 8) L.ST = 8;
     if (cap_ring && L.ST > blocks_per_cta) L.ST = static_cast<int>(blocks_per_cta < 2 ? 2 : blocks_per_cta);
@@ -515,9 +521,9 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
             return cudaErrorInvalidValue;
     }
     // codes of each linear: uint8 [N][K/2]; full tiles load 128 rows x 128 bytes (4 groups) with the
-    // 128-byte swizzle, partial tiles r_rem rows x 32 * load_span(s_rem) * s_rem bytes
+    // 128-byte swizzle, partial tiles r_rem rows x 32 * box_span(s_rem) * s_rem bytes
     st::CodeMaps cm = {};
-    const uint32_t rem_bytes = 32u * st::load_span(P.s_rem) * P.s_rem;
+    const uint32_t rem_bytes = 32u * st::box_span(P.s_rem) * P.s_rem;
     for (int i = 0; i < P.count; i++) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(P.n[i])};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};

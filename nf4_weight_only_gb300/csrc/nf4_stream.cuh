@@ -21,11 +21,12 @@
 // CTA with only a dozen rows still fill all 128 MMA rows and all 128 dequant lanes, so the grid is
 // one CTA per SM with a balanced row range each, for any N.
 //
-// Rings.  Codes move in load stages of U k-stages (one TMA box of all rows x U*S groups, 128 bytes a
-// row where possible: the TMA engine moves short rows slowly); x moves per k-stage (one box of T
-// tokens x S groups); scales per 8 k-stages (zero-filling 16-byte copies of each row's window).  The
-// codes ring is released by the dequant warps, the x ring by the MMAs, and the tensor-memory ring of
-// A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
+// Rings.  Codes move in load stages of U 64-k sub-stages (U = 4 for S = 1, else 2; one TMA box of
+// all rows x U*S groups, 128 bytes a row where possible: the TMA engine moves short rows slowly;
+// two boxes of 32*S-byte rows for S >= 3); x moves per sub-stage (one box of T tokens x S groups);
+// scales per 8 sub-stages (zero-filling 16-byte copies of each row's window).  The codes and scale
+// rings are released by the dequant sets whose stages read them, the x ring by the MMAs, and the
+// tensor-memory ring of A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
 //
 // Warp roles: warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp copies
 // scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2 .. 4*S+1 are S sets of
@@ -98,8 +99,14 @@ struct Cfg {
                   "barrier area");
 };
 
-// k-stages per codes load stage for a tile of S slices: 128 bytes a row for S = 1, 2, 4.
-__host__ __device__ constexpr int load_span(int s) { return s == 1 ? 4 : (s == 2 ? 2 : 1); }
+// 64-k sub-stages per TMA box of codes for a tile of S slices: 128-byte rows for S = 1 and 2,
+// 32 * S bytes for S >= 3.
+__host__ __device__ constexpr int box_span(int s) { return s == 1 ? 4 : (s == 2 ? 2 : 1); }
+// Sub-stages per codes load stage: four for S = 1, two otherwise (two boxes for S >= 3, each at its
+// own 8 KB half of the slot).  A load stage thus never holds less than one whole pipeline stage,
+// which keeps a dequant set's consecutive load stages at most kSets apart (see the dequant loop).
+__host__ __device__ constexpr int load_span(int s) { return s == 1 ? 4 : 2; }
+constexpr uint32_t kBoxStride = 8192;  // second box of a load stage (a box is <= 128 rows x 32 bytes)
 
 struct Params {
     const uint8_t* codes[kMaxProblems];
@@ -257,13 +264,13 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
 
     // barriers
     const uint32_t b_lfull = sbase + C::kOffBars;       // [NL] codes load stage landed (tx)
-    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage seen and read (every dequant warp)
+    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage read (its stages' sets)
     const uint32_t b_xfull = b_lempty + 8 * NL;         // [NX] x tile landed (tx)
     const uint32_t b_xempty = b_xfull + 8 * NX;         // [NX] x tile read by the MMAs (commit)
     const uint32_t b_afull = b_xempty + 8 * NX;         // [NA] A tile in tensor memory (4 warps)
     const uint32_t b_aempty = b_afull + 8 * NA;         // [NA] A tile read by the MMAs (commit)
     const uint32_t b_sfull = b_aempty + 8 * NA;         // [NSS] scale tile landed (32 producer lanes)
-    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile seen and read (every dequant warp)
+    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile read (its stages' sets)
     // accumulators complete (commit), one barrier per epilogue set: a set waits only for its own
     // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
     const uint32_t b_dfull = b_sempty + 8 * NSS;        // [kSets]
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NL; i++) {
             mbar_init(b_lfull + 8 * i, 1);
-            mbar_init(b_lempty + 8 * i, 4 * C::kSets);  // every dequant warp releases every load stage
+            mbar_init(b_lempty + 8 * i, 8);  // weighted releases of the stages that read it
         }
         for (int i = 0; i < NX; i++) {
             mbar_init(b_xfull + 8 * i, 1);
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         }
         for (int i = 0; i < NSS; i++) {
             mbar_init(b_sfull + 8 * i, 32);
-            mbar_init(b_sempty + 8 * i, 4 * C::kSets);
+            mbar_init(b_sempty + 8 * i, 48);
         }
         for (int i = 0; i < C::kSets; i++) {
             mbar_init(b_dfull + 8 * i, 1);
@@ -342,7 +349,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const Tile t = tile_of(P, rbeg, rows_cta, j);
             const int U = load_span(t.s);
             const CUtensorMap* cmap = t.s > 1 ? cm_rem : cm_full;
-            const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;
+            const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;  // all boxes of a stage
+            const int BS = box_span(t.s);
             const uint32_t per_row = (t.s + 2) * 16;
             for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
                 if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
@@ -353,8 +361,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     }
                     if (lane == 0) {
                         mbar_expect_tx(b_lfull + 8 * lslot, cbytes);
-                        tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes, cmap, g * 32, t.row0,
-                                    b_lfull + 8 * lslot);
+                        for (int b = 0; b < U / BS; b++)
+                            tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes + b * kBoxStride, cmap,
+                                        (g + b * BS * t.s) * 32, t.row0, b_lfull + 8 * lslot);
                     }
                     lq++;
                     if (++lslot == NL) {
@@ -492,38 +501,24 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
         // ring slots and phases follow from them, so a set visits only its own stages.
         int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
-        // A parity wait names one of two phases, so it is sound only while the barrier is neither a
-        // phase behind (this warp saw the previous fill of the slot) nor a phase ahead (the producer
-        // refilled the slot before this warp saw it).  Hence every warp sees every codes load stage
-        // and scale tile in the producer's own order (by sub-stage: the load stage, then the scale
-        // tile), and releases each exactly once: at the end of its last stage that reads it, or at
-        // once if its set reads none of it.  A warp never waits while holding a slot the producer
-        // needs first, so the rings cannot deadlock.
-        int kobs = 0;  // next sub-stage of tile j whose load stage / scale tile this warp has to see
-        int U = 1;
-        auto see = [&](int kend, int lkeep, int skeep) {  // see sub-stages kobs .. kend; release
-            bool good = true;                              // load stages < lkeep, scale tiles < skeep
-            for (; good && kobs <= kend; kobs++) {
-                if ((kobs & (U - 1)) == 0) {
-                    const int L = l0 + kobs / U;
-                    good = warp_wait(b_lfull + 8 * (L % NL), (L / NL) & 1, deadline);
-                    if (good && kobs / U < lkeep && lane == 0) mbar_arrive(b_lempty + 8 * (L % NL));
-                }
-                if (good && (kobs & 7) == 0) {
-                    const int S = s0 + kobs / 8;
-                    good = warp_wait(b_sfull + 8 * (S % NSS), (S / NSS) & 1, deadline);
-                    if (good && kobs / 8 < skeep && lane == 0) mbar_arrive(b_sempty + 8 * (S % NSS));
-                }
-            }
-            return good;
-        };
+        // A warp waits only for the codes load stage and the scale tile of its own stages, and its
+        // set releases them after use; the release counts are weighted so that a slot completes when
+        // every stage that reads it is done (a load stage: 8 = two stages of four warps, or one at
+        // weight 2; a scale tile: 48 = n stages of four warps at weight 12 / n).  A parity wait is
+        // sound when the slot's previous fill has completed and its next cannot have: the next
+        // needs this warp's own release, and the previous is complete once the fills are at most
+        // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
+        // A set's stages are kSets apart; a load stage holds two stages (S = 1, the only case of the
+        // wide tiles) or one, and a scale tile four.
+        static_assert((C::kWide ? (C::kSets + 1) / 2 : C::kSets) <= NL && C::kSets <= 4 && NSS >= 2,
+                      "ring too shallow for the release rule");
+        static_assert(!C::kWide || C::kSMax == 1, "wide tiles have one K-slice (four sub-stages per load stage)");
         for (int j = 0; j < ntiles && ok; j++) {
             q0 += nst_prev;
             l0 += nload_prev;
             s0 += nscale_prev;
             const Tile t = tile_of(P, rbeg, rows_cta, j);
-            U = load_span(t.s);
-            kobs = 0;
+            const int U = load_span(t.s), BS = box_span(t.s);
             const int nst = t.nt / 2, nload = (t.nt + U - 1) / U, nscale = (t.nt + 7) / 8;
             nst_prev = nst;
             nload_prev = nload;
@@ -531,9 +526,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const int r = i / t.s, sl = i - (i / t.s) * t.s;
             const bool lane_ok = r < t.rows;
             const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
-            // codes of row r in a load stage: rowb bytes, 16-byte chunks permuted by the 128-byte
-            // swizzle (chunk ^ (r mod 8)) when the row is 128 bytes
-            const uint32_t rowb = 32u * U * t.s;
+            // codes of row r in a box: rowb bytes, 16-byte chunks permuted by the 128-byte swizzle
+            // (chunk ^ (r mod 8)) when the row is 128 bytes
+            const uint32_t rowb = 32u * BS * t.s;
             const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
             // this lane's scale inside a scale tile: row r's window starts at the 16-byte boundary
             // below its first scale; sub-stage kb adds 2 * (kb mod 8) * S bytes
@@ -544,10 +539,12 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 const int gq = q0 + kb2;
                 const int aslot = gq % NA, around = gq / NA;
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
-                const int lfirst = kbs / U, llast = (kbs + 1) / U;  // its codes load stage(s), tile-relative
+                const int li = kbs / U;                   // its codes load stage, tile-relative
                 const int si = kbs / 8;                   // its scale tile, tile-relative
-                const int sslot = (s0 + si) % NSS;
-                bool good = see(kbs + 1, lfirst, si);
+                const int L = l0 + li, S = s0 + si;       // CTA-wide
+                const int lslot = L % NL, sslot = S % NSS;
+                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, deadline) &&
+                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, deadline);
                 if (good && around > 0) good = warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline);
                 if (!good) {
                     record_error(26);
@@ -559,13 +556,12 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
                     if (!warp_ok) break;
                     const int kb = kbs + h;
-                    const int u = kb & (U - 1);
-                    const int lslot = (l0 + kb / U) % NL;
+                    const int u = kb & (U - 1);           // sub-stage in the load stage: box u / BS
                     uint32_t out[32];
                     const int g = kb * t.s + sl;
                     if (lane_ok && g < G) {
-                        const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + r * rowb;
-                        const uint32_t ch = static_cast<uint32_t>((u * t.s + sl) * 2);
+                        const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + (u / BS) * kBoxStride + r * rowb;
+                        const uint32_t ch = static_cast<uint32_t>(((u % BS) * t.s + sl) * 2);
                         const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
                         const uint16_t sc = *reinterpret_cast<const uint16_t*>(
                             smem + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s);
@@ -613,19 +609,11 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(b_afull + 8 * aslot);
-                    // a set never reads a load stage in two of its stages (kSets >= 2), so the stage's
-                    // load stages go back now; its scale tile (4 stages) only after the set's last
-                    // stage in it
-                    for (int li = lfirst; li <= llast; li++) mbar_arrive(b_lempty + 8 * ((l0 + li) % NL));
-                    const int nxt = kb2 + C::kSets;
-                    if (nxt >= nst || (2 * nxt) / 8 != si) mbar_arrive(b_sempty + 8 * sslot);
+                    const int touching = U == 4 ? (nst - 2 * li < 2 ? nst - 2 * li : 2) : 1;
+                    mbar_arrive_count(b_lempty + 8 * lslot, 2 / touching);
+                    const int stouch = nst - 4 * si < 4 ? nst - 4 * si : 4;
+                    mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
                 }
-            }
-            // see and release the rest of tile j, so that no warp holds a slot that the other sets
-            // still need while it waits for the accumulators or moves on to the next tile
-            if (ok && !see(t.nt - 1, nload, nscale)) {
-                record_error(26);
-                ok = false;
             }
             if (!ok || j % C::kSets != set) continue;
             // ------------------------------------------------------------ epilogue of tile j
