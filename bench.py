@@ -228,6 +228,7 @@ def run_ours(args, rank, world):
 
     prefill = prefill_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
     embed = embed_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
+    codec = codec_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
     overflow = overflow_bench(nf4, synth, dev) if not args.skip_prefill else None
 
     result = {
@@ -254,6 +255,8 @@ def run_ours(args, rank, world):
         result["prefill"] = prefill
     if embed is not None:
         result["embed"] = embed
+    if codec is not None:
+        result.update(codec)  # "quantize" and "dequant"
     if overflow is not None:
         result["overflow"] = overflow
     return result
@@ -347,6 +350,43 @@ def embed_bench(nf4, synth, dev, pk, vocab: int = 151936, hidden: int = 2048, n_
             "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "us": round(t * 1e6, 2),
             "algorithmic_bytes": algo, "kernel": "embed_kernel", "l2": "flushed (256 MB written) before each launch",
             "clocks": clocks_summary(samples)}
+
+
+def codec_bench(nf4, synth, dev, pk, n: int = 16384, k: int = 16384):
+    """GB/s of `nf4_quantize` (fp32 in, codes + scales out: 4.53 B/weight) and `nf4_dequant` (codes +
+    scales in, bf16 out: 2.53 B/weight) on one n x k matrix; every buffer is larger than L2."""
+    w = synth.device_weights(41, n, k, dev)
+    codes = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, k // 64), dtype=torch.float16, device=dev)
+    w_hat = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    out = {}
+    for name, call, algo in (
+            ("quantize", lambda: nf4.nf4_quantize(w, codes, scales, stream), n * k * 4 + n * k // 2 + n * (k // 64) * 2),
+            ("dequant", lambda: nf4.nf4_dequant(codes, scales, w_hat, stream), n * k // 2 + n * (k // 64) * 2 + n * k * 2)):
+        iters = 20
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+            for a, b in evs:
+                a.record(stream)
+                call()
+                b.record(stream)
+        samples = []
+        while not evs[-1][1].query():
+            samples.append(sample_clocks(dev.index))
+        torch.cuda.synchronize()
+        t = statistics.median(a.elapsed_time(b) / 1e3 for a, b in evs)
+        gbs = algo / t / 1e9
+        out[name] = {"workload": f"{n} x {k} matrix", "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                     "us": round(t * 1e6, 2), "algorithmic_bytes": algo,
+                     "kernel": "quantize_kernel" if name == "quantize" else "dequant_kernel",
+                     "l2": "every buffer larger than L2", "clocks": clocks_summary(samples)}
+    del w, codes, scales, w_hat
+    torch.cuda.empty_cache()
+    return out
 
 
 def prefill_bench(nf4, synth, dev, pk):
@@ -453,19 +493,40 @@ def profile_linear(m: int, n: int, k: int) -> None:
     print(f"profile-linear M={m} N={n} K={k}: ok, device error word {nf4.nf4_check_device_error()}")
 
 
+def profile_codec(n: int, k: int) -> None:
+    """Quantize one random n x k matrix on the device and dequantize it, twice each, for profiler
+    captures of the two codec kernels; prints nothing to time."""
+    import nf4_weight_only_gb300 as nf4
+    from nf4_weight_only_gb300 import build, synth
+    build.build()
+    nf4.load()
+    dev = torch.device("cuda", 0)
+    w = synth.device_weights(41, n, k, dev)
+    for _ in range(2):
+        codes, scales = nf4.quantize(w)
+        w_hat = nf4.dequant(codes, scales)
+    torch.cuda.synchronize()
+    print(f"profile-codec N={n} K={k}: ok, {w_hat.shape[0]} rows")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill and embedding lines")
+    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill, embedding, codec and overflow lines")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-codec", nargs=2, type=int, metavar=("N", "K"),
+                    help="quantize and dequantize one N x K matrix (for single-kernel profiler captures)")
     ap.add_argument("--profile-linear", nargs=3, type=int, metavar=("M", "N", "K"),
                     help="run one M x N x K linear four times (for single-kernel profiler captures) and exit")
     args = ap.parse_args()
     if args.profile_linear:
         profile_linear(*args.profile_linear)
+        return
+    if args.profile_codec:
+        profile_codec(*args.profile_codec)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -49,7 +49,11 @@ __device__ __forceinline__ uint32_t code_of(float r, const float* thr) {
     return c;
 }
 
-// One warp per group: lane l holds weights 2l and 2l+1 and writes code byte l.
+// A warp takes kQuantGroups consecutive groups per step and issues all their loads before it
+// computes any of them (one 256-byte load per group would leave too few bytes in flight for HBM).
+// Within a group, lane l holds weights 2l and 2l+1 and writes code byte l.
+constexpr int kQuantGroups = 8;
+
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ w, int64_t groups,
                                                        uint8_t* __restrict__ codes,
                                                        uint16_t* __restrict__ scales) {
@@ -58,24 +62,36 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < groups;
-         g += warps) {
-        const float2 v = __ldcs(reinterpret_cast<const float2*>(w + g * kGroup) + lane);
-        float s = fmaxf(fabsf(v.x), fabsf(v.y));
+    for (int64_t g0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kQuantGroups;
+         g0 < groups; g0 += warps * kQuantGroups) {
+        float2 v[kQuantGroups];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
-        uint32_t byte = 0x77u;  // an all-zero group: code 7 (T[7] = 0) everywhere
-        if (s != 0.0f) {
-            const uint32_t c0 = code_of(__fdiv_rn(v.x, s), thr);
-            const uint32_t c1 = code_of(__fdiv_rn(v.y, s), thr);
-            byte = c0 | (c1 << 4);
+        for (int j = 0; j < kQuantGroups; j++)
+            v[j] = g0 + j < groups ? __ldcs(reinterpret_cast<const float2*>(w + (g0 + j) * kGroup) + lane)
+                                   : make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < kQuantGroups; j++) {
+            const int64_t g = g0 + j;
+            if (g >= groups) break;  // warp-uniform
+            float s = fmaxf(fabsf(v[j].x), fabsf(v[j].y));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+            uint32_t byte = 0x77u;  // an all-zero group: code 7 (T[7] = 0) everywhere
+            if (s != 0.0f) {
+                const uint32_t c0 = code_of(__fdiv_rn(v[j].x, s), thr);
+                const uint32_t c1 = code_of(__fdiv_rn(v[j].y, s), thr);
+                byte = c0 | (c1 << 4);
+            }
+            codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte);
+            if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s));
         }
-        codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte);
-        if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s));
     }
 }
 
-// Each thread expands 8 code bytes (16 weights, a quarter group) into 32 bytes of bf16.
+// Each thread expands 8 code bytes (16 weights, a quarter group) into 32 bytes of bf16, for
+// kDequantQuarters quarters per step whose loads it issues first.
+constexpr int kDequantQuarters = 4;
+
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ codes,
                                                       const uint16_t* __restrict__ scales, int64_t groups,
                                                       uint16_t* __restrict__ w_hat) {
@@ -84,20 +100,34 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
     __syncthreads();
     const int64_t quarters = groups * 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < quarters; q += stride) {
-        const uint2 cw = __ldcs(reinterpret_cast<const uint2*>(codes) + q);
-        const float s = __half2float(__ushort_as_half(scales[q >> 2]));
-        uint32_t out[8];
+    // step i of a thread covers quarters q0 + u * stride, u < kDequantQuarters (coalesced per u)
+    for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q0 < quarters;
+         q0 += stride * kDequantQuarters) {
+        uint2 cw[kDequantQuarters];
+        uint16_t sc[kDequantQuarters];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const uint32_t byte = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
-            const uint32_t lo = bf16_bits(__fmul_rn(table[byte & 0xFu], s));
-            const uint32_t hi = bf16_bits(__fmul_rn(table[byte >> 4], s));
-            out[j] = lo | (hi << 16);
+        for (int u = 0; u < kDequantQuarters; u++) {
+            const int64_t q = q0 + u * stride;
+            cw[u] = q < quarters ? __ldcs(reinterpret_cast<const uint2*>(codes) + q) : make_uint2(0, 0);
+            sc[u] = q < quarters ? scales[q >> 2] : static_cast<uint16_t>(0);
         }
-        uint4* dst = reinterpret_cast<uint4*>(w_hat + q * 16);
-        __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-        __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+#pragma unroll
+        for (int u = 0; u < kDequantQuarters; u++) {
+            const int64_t q = q0 + u * stride;
+            if (q >= quarters) break;
+            const float s = __half2float(__ushort_as_half(sc[u]));
+            uint32_t out[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t byte = ((j < 4 ? cw[u].x : cw[u].y) >> (8 * (j & 3))) & 0xFFu;
+                const uint32_t lo = bf16_bits(__fmul_rn(table[byte & 0xFu], s));
+                const uint32_t hi = bf16_bits(__fmul_rn(table[byte >> 4], s));
+                out[j] = lo | (hi << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(w_hat + q * 16);
+            __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
+            __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+        }
     }
 }
 
@@ -154,7 +184,7 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes
                             int num_sms, cudaStream_t stream) {
     const int64_t groups = N * (K / kGroup);
     if (groups == 0) return cudaSuccess;
-    const int grid = grid_for(8, groups, num_sms, 8);  // 8 warps (groups) per 256-thread block
+    const int grid = grid_for(8 * kQuantGroups, groups, num_sms, 8);  // 8 warps per 256-thread block
     quantize_kernel<<<grid, 256, 0, stream>>>(w, groups, codes, scales);
     return cudaGetLastError();
 }
@@ -163,7 +193,7 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t
                            uint16_t* w_hat, int num_sms, cudaStream_t stream) {
     const int64_t groups = N * (K / kGroup);
     if (groups == 0) return cudaSuccess;
-    const int grid = grid_for(256, groups * 4, num_sms, 8);
+    const int grid = grid_for(256 * kDequantQuarters, groups * 4, num_sms, 8);
     dequant_kernel<<<grid, 256, 0, stream>>>(codes, scales, groups, w_hat);
     return cudaGetLastError();
 }
