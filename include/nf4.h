@@ -30,6 +30,10 @@
  *     M, N and K must each be at most 2^31 - 1.
  *   - Non-finite inputs are outside the contract: results are unspecified, but no call faults.
  *   - The same inputs give the same output bytes on every call (no atomics, fixed reduction order).
+ *   - Every entry point except the ring calls (see their section) may be called from several host
+ *     threads at once, on the same or different streams: the only shared state is the per-device
+ *     capability cache (atomic), one-time kernel attributes (std::call_once) and the per-device
+ *     constant table, built once under a mutex.
  */
 #ifndef NF4_H
 #define NF4_H

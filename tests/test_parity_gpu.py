@@ -211,6 +211,55 @@ def test_linear_deterministic(nf4, o):
     assert np.array_equal(y1, y2)
 
 
+def test_concurrent_host_threads_and_streams(nf4, o):
+    """Four host threads, each with its own stream, run the GEMV (M = 1, 3), the T <= 32 streaming
+    kernel (M = 8), the wide one (M = 300) and a grouped launch ten times each, all at once: every
+    result equals the single-threaded one bit for bit (ctypes releases the GIL around the calls)."""
+    import threading
+    from nf4_weight_only_gb300 import synth
+    cases = [(1, 4096, 2048, 0), (3, 1536, 11008, 1), (8, 6144, 5120, 2), (300, 1024, 2048, 3)]
+    prepared = []
+    for m, n, k, seed in cases:
+        codes, scales = nf4.quantize(synth.device_weights(900 + seed, n, k, DEV))
+        x = synth.device_activations_bf16(950 + seed, m, k, DEV)
+        ref = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+        nf4.nf4_linear(x, codes, scales, ref)
+        prepared.append((x, codes, scales, ref))
+    gx = prepared[1][0]
+    g_ref = [torch.empty((3, n), dtype=torch.bfloat16, device=DEV) for n in (1536, 512)]
+    g_mats = [(prepared[1][1], prepared[1][2]), nf4.quantize(synth.device_weights(990, 512, 11008, DEV))]
+    nf4.nf4_linear_grouped(gx, [c for c, _ in g_mats], [s for _, s in g_mats], g_ref)
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            stream = torch.cuda.Stream(device=DEV)
+            x, codes, scales, ref = prepared[i]
+            outs = [torch.empty_like(ref) for _ in range(10)]
+            g_outs = [[torch.empty_like(r) for r in g_ref] for _ in range(10)]
+            for j in range(10):
+                nf4.nf4_linear(x, codes, scales, outs[j], stream)
+                nf4.nf4_linear_grouped(gx, [c for c, _ in g_mats], [s for _, s in g_mats], g_outs[j], stream)
+            stream.synchronize()
+            for j in range(10):
+                if not torch.equal(outs[j].view(torch.int16), ref.view(torch.int16)):
+                    errors.append(f"thread {i} call {j}: linear differs")
+                for a, b in zip(g_outs[j], g_ref):
+                    if not torch.equal(a.view(torch.int16), b.view(torch.int16)):
+                        errors.append(f"thread {i} call {j}: grouped differs")
+        except Exception as e:  # reported below
+            errors.append(f"thread {i}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:5]
+    assert device_error(nf4) == 0
+
+
 def test_empty_is_noop(nf4):
     y = torch.full((4,), 7.0, dtype=torch.bfloat16, device=DEV)
     x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
