@@ -51,7 +51,10 @@ __device__ __forceinline__ uint32_t code_of(float r, const float* thr) {
 
 // A warp takes kQuantGroups consecutive groups per step and issues all their loads before it
 // computes any of them (one 256-byte load per group would leave too few bytes in flight for HBM).
-// Within a group, lane l holds weights 2l and 2l+1 and writes code byte l.
+// Within a group, lane l holds weights 2l and 2l+1 and writes code byte l.  The groups' steps carry
+// no branches, so their reductions, divisions and searches interleave: an all-zero group divides by
+// 1 instead of by s = 0, which turns its weights (+0 or -0) into r = +-0, whose code is 7 (T[7] = 0)
+// as the format requires.
 constexpr int kQuantGroups = 8;
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ w, int64_t groups,
@@ -65,25 +68,32 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
     for (int64_t g0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kQuantGroups;
          g0 < groups; g0 += warps * kQuantGroups) {
         float2 v[kQuantGroups];
+        float s[kQuantGroups];
 #pragma unroll
-        for (int j = 0; j < kQuantGroups; j++)
+        for (int j = 0; j < kQuantGroups; j++) {
             v[j] = g0 + j < groups ? __ldcs(reinterpret_cast<const float2*>(w + (g0 + j) * kGroup) + lane)
                                    : make_float2(0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < kQuantGroups; j++) s[j] = fmaxf(fabsf(v[j].x), fabsf(v[j].y));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int j = 0; j < kQuantGroups; j++) s[j] = fmaxf(s[j], __shfl_xor_sync(0xFFFFFFFFu, s[j], o));
+        }
+        uint32_t byte[kQuantGroups];
+#pragma unroll
+        for (int j = 0; j < kQuantGroups; j++) {
+            const float d = s[j] != 0.0f ? s[j] : 1.0f;
+            byte[j] = code_of(__fdiv_rn(v[j].x, d), thr) | (code_of(__fdiv_rn(v[j].y, d), thr) << 4);
+        }
 #pragma unroll
         for (int j = 0; j < kQuantGroups; j++) {
             const int64_t g = g0 + j;
-            if (g >= groups) break;  // warp-uniform
-            float s = fmaxf(fabsf(v[j].x), fabsf(v[j].y));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
-            uint32_t byte = 0x77u;  // an all-zero group: code 7 (T[7] = 0) everywhere
-            if (s != 0.0f) {
-                const uint32_t c0 = code_of(__fdiv_rn(v[j].x, s), thr);
-                const uint32_t c1 = code_of(__fdiv_rn(v[j].y, s), thr);
-                byte = c0 | (c1 << 4);
+            if (g < groups) {
+                codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte[j]);
+                if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s[j]));
             }
-            codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte);
-            if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s));
         }
     }
 }

@@ -48,6 +48,8 @@ def test_quantize_bit_exact(nf4, o, n, k, seed, outliers):
     from nf4_weight_only_gb300 import synth
     w = synth.weights(seed, n, k, outlier_frac=outliers)
     w[0, :64] = 0.0                # an all-zero group
+    if k >= 128:
+        w[0, 64:128] = -0.0        # an all-zero group of negative zeros (code 7 as well)
     if n > 1:
         w[1, 64:128] *= 1e-6       # tiny scale (fp16 subnormal range)
     codes, scales = gpu_quantize(nf4, w)
