@@ -230,11 +230,22 @@ nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* codes, cons
 /*
  * nf4_check_device_error - diagnostics: read and clear the device-side error words of the current
  * device.  The linear kernels bound every pipeline wait (about one second); a wait that runs out
- * records a nonzero code (1..39), and the kernel drains and exits instead of hanging.  nf4_embed
+ * records a nonzero code (1..39; 39 is nf4_diag_bounded_wait's), and the kernel drains and exits
+ * instead of hanging.  nf4_embed
  * records 41 for an id outside the table.  *code receives the first recorded code (0 = none).
  * This call waits for the device (it is not meant for the hot path).
  */
 nf4_status nf4_check_device_error(int* code);
+
+/*
+ * nf4_diag_bounded_wait - diagnostics, no counterpart in the pages: checks that a pipeline wait
+ * which runs out reports instead of hanging.  Launches one thread on `stream` that waits on an
+ * mbarrier nothing ever arrives on, through the same bounded wait and error word as the linear
+ * kernels; after `cycles` SM clocks it gives up and records code 39, which nf4_check_device_error
+ * then returns.  The device stays usable.  cycles must be in [1, 2^31] (about one second at the
+ * GB300's top clock), else NF4_ERR_SHAPE.
+ */
+nf4_status nf4_diag_bounded_wait(int64_t cycles, cudaStream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* nf4_status_str(nf4_status status);

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_
 # Every symbol include/nf4.h declares.
 EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_embed",
             "nf4_ring_create", "nf4_ring_run", "nf4_ring_destroy", "nf4_linear_host_noalloc",
-            "nf4_check_device_error", "nf4_status_str", "nf4_abi_version")
+            "nf4_check_device_error", "nf4_diag_bounded_wait", "nf4_status_str", "nf4_abi_version")
 
 
 class HostLinear(ctypes.Structure):
@@ -75,6 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_status_str.restype = ctypes.c_char_p
     lib.nf4_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.nf4_check_device_error.restype = ci
+    lib.nf4_diag_bounded_wait.argtypes = [i64, vp]
+    lib.nf4_diag_bounded_wait.restype = ci
     lib.nf4_abi_version.argtypes = []
     lib.nf4_abi_version.restype = ci
     if path is None:
@@ -211,6 +213,12 @@ def nf4_linear_host_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.
     n = codes.shape[0]
     _check(load().nf4_linear_host_noalloc(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
            "nf4_linear_host_noalloc")
+
+
+def nf4_diag_bounded_wait(cycles: int, stream=None) -> None:
+    """Launch one thread whose bounded wait on a barrier nothing arrives on runs out after `cycles`
+    SM clocks and records code 39 in the device error word (diagnostics)."""
+    _check(load().nf4_diag_bounded_wait(int(cycles), _stream(stream)), "nf4_diag_bounded_wait")
 
 
 def nf4_check_device_error() -> int:

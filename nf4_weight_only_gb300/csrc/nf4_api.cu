@@ -155,6 +155,14 @@ nf4_status nf4_check_device_error(int* code) {
     return NF4_OK;
 }
 
+nf4_status nf4_diag_bounded_wait(int64_t cycles, cudaStream_t stream) {
+    if (cycles <= 0 || cycles > (int64_t{1} << 31)) return NF4_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    nf4_status st = current_device(&dev, &sms);
+    if (st != NF4_OK) return st;
+    return from_cuda(nf4::launch_diag_wait(cycles, stream));
+}
+
 nf4_status nf4_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
                      int64_t K, uint16_t* out, cudaStream_t stream) {
     if (n_ids < 0 || V < 0 || n_ids > kMaxDim || V > kMaxDim) return NF4_ERR_SHAPE;

@@ -656,6 +656,23 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
     return launch_stream_t<32>(x, P, M, K, stream);
 }
 
+// One thread waits on an mbarrier that nothing arrives on, with the pipelines' bounded wait and
+// error word: after `cycles` SM clocks the wait gives up and records 39 (the check of a timed-out
+// wait's reporting path; no fault, no hang).
+__global__ void diag_wait_kernel(long long cycles) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait(b, 0, clock64() + cycles)) record_error(39);
+}
+
+cudaError_t launch_diag_wait(int64_t cycles, cudaStream_t stream) {
+    diag_wait_kernel<<<1, 32, 0, stream>>>(static_cast<long long>(cycles));
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_error(int* code) {
     int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int));

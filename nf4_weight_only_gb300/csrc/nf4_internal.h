@@ -30,6 +30,7 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
                           cudaStream_t stream);
 // Device error word of the linear kernels (nonzero after a bounded pipeline wait timed out).
 cudaError_t read_and_clear_error(int* code);
+cudaError_t launch_diag_wait(int64_t cycles, cudaStream_t stream);
 
 // Packed embedding rows (out-of-range ids write zeros and set the embed error word to 41).
 cudaError_t launch_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,

@@ -103,6 +103,13 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
     assert linear(lib, A, B, C, D, 1, 4, 64) in (5, 6)
 
 
+def test_diag_wait_rejects_unbounded_limits(lib):
+    """The diagnostic wait takes a limit in [1, 2^31] SM clocks; anything else is rejected on the host."""
+    lib.nf4_diag_bounded_wait.argtypes = [ctypes.c_int64, vp]
+    for cycles in (0, -1, (1 << 31) + 1, 1 << 62):
+        assert lib.nf4_diag_bounded_wait(cycles, None) == 2  # NF4_ERR_SHAPE
+
+
 def test_binding_raises_without_library(tmp_path):
     import nf4_weight_only_gb300 as nf4
     with pytest.raises(RuntimeError, match="missing"):

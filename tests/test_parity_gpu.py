@@ -262,6 +262,18 @@ def test_concurrent_host_threads_and_streams(nf4, o):
     assert device_error(nf4) == 0
 
 
+def test_timed_out_wait_reports_and_device_stays_usable(nf4, o):
+    """A bounded wait that runs out (one thread on a barrier nothing arrives on, about 1 ms) records
+    code 39 instead of hanging; the next linear on the same device is still correct."""
+    nf4.nf4_diag_bounded_wait(2_000_000)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 39
+    assert device_error(nf4) == 0  # reading clears the word
+    check_linear(nf4, o, 1, 257, 2048, seed=5)
+    check_linear(nf4, o, 8, 130, 192, seed=6)
+    assert device_error(nf4) == 0
+
+
 def test_empty_is_noop(nf4):
     y = torch.full((4,), 7.0, dtype=torch.bfloat16, device=DEV)
     x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
