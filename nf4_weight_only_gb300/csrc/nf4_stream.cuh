@@ -29,11 +29,12 @@
 // tensor-memory ring of A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
 //
 // Warp roles: warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp copies
-// scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2 .. 4*S+1 are S sets of
-// four dequant warps (a set takes every S-th stage; the four warps of a set cover the four 32-lane
-// quarters of tensor memory) that also run the epilogue of every S-th tile, and the last warp
-// streams x.  S = 4 for the wide tiles (608 threads) and 3 for T <= 32 (480 threads): with fewer
-// sets the lookups' dependent integer chains leave the dequant warps latency-bound.
+// scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2 .. 4*kSets+1 are kSets
+// sets of four dequant warps (a set takes every kSets-th stage and waits only for the codes and
+// scales of its own stages; the four warps of a set cover the four 32-lane quarters of tensor
+// memory) that also run the epilogue of every kSets-th tile, and the last warp streams x.
+// kSets = 4 for the wide tiles (608 threads) and 3 for T <= 32 (480 threads): with fewer sets the
+// lookups' dependent integer chains leave the dequant warps latency-bound.
 // Weights do not depend on the previous kernel in the stream, so warp 0 never waits for it; only x
 // and y do.  Each producer runs as far ahead as its own ring allows.
 //
