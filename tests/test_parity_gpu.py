@@ -262,6 +262,49 @@ def test_concurrent_host_threads_and_streams(nf4, o):
     assert device_error(nf4) == 0
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 3, (1 << 26) + 192), (3, 2, (1 << 24) + 64)])
+def test_linear_huge_k(nf4, o, m, n, k):
+    """K of 16.8 M and 67.1 M (ragged past a power of two): the streaming kernel's group, box and
+    scale-window arithmetic at sizes where a 32-bit byte offset of a row's scales would overflow."""
+    from nf4_weight_only_gb300 import synth
+    w = synth.device_weights(700 + n, n, k, DEV)
+    codes, scales = nf4.quantize(w)
+    x = synth.device_activations_bf16(701 + n, m, k, DEV)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    nf4.nf4_linear(x, codes, scales, y)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    c_ref, s_ref = o.quantize(w.cpu().numpy())
+    del w
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(f16_dev_to_bits(scales), s_ref)
+    y64, mag = o.linear(dev_to_bits(x), c_ref, s_ref, nthreads=16)
+    ok, ratio, mask = oracle.within_tolerance(dev_to_bits(y), y64, mag)
+    assert ok, f"M={m} N={n} K={k}: worst ratio {ratio:.3f}"
+
+
+def test_linear_five_million_rows(nf4, o):
+    """N = 5,000,000 rows of K = 64 at M = 1 (the GEMV's row-range split over the whole grid);
+    4096 sampled rows, the first and the last included, checked against the oracle."""
+    from nf4_weight_only_gb300 import synth
+    n, k = 5_000_000, 64
+    w = synth.device_weights(720, n, k, DEV)
+    codes, scales = nf4.quantize(w)
+    x = synth.device_activations_bf16(721, 1, k, DEV)
+    y = torch.empty((1, n), dtype=torch.bfloat16, device=DEV)
+    nf4.nf4_linear(x, codes, scales, y)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    rng = np.random.default_rng(722)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 4094)]))
+    sel = torch.from_numpy(rows.astype(np.int64)).to(DEV)
+    c_ref, s_ref = o.quantize(w[sel].cpu().numpy())
+    assert np.array_equal(codes[sel].cpu().numpy(), c_ref)
+    y64, mag = o.linear(dev_to_bits(x), c_ref, s_ref, nthreads=16)
+    ok, ratio, mask = oracle.within_tolerance(dev_to_bits(y)[:, rows], y64, mag)
+    assert ok, f"{np.count_nonzero(~mask)} sampled rows outside tolerance (worst {ratio:.3f})"
+
+
 def test_timed_out_wait_reports_and_device_stays_usable(nf4, o):
     """A bounded wait that runs out (one thread on a barrier nothing arrives on, about 1 ms) records
     code 39 instead of hanging; the next linear on the same device is still correct."""
