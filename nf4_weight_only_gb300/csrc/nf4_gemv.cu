@@ -568,6 +568,20 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
                           uint16_t* const* ys, const int64_t* Ns, int64_t M, int64_t K, int num_sms,
                           cudaStream_t stream) {
     if (count < 1 || count > st::kMaxProblems || M < 1 || num_sms < 1) return cudaErrorInvalidValue;
+    // Token tiles run along the grid's y dimension (at most 65535 of them): a larger M goes in
+    // chunks of that many 256-token tiles, each with x and every y offset by the chunk's first
+    // token (offsets of whole rows keep the 16-byte alignment the kernels rely on).
+    constexpr int64_t kTokensPerLaunch = 65535LL * 256;
+    if (M > kTokensPerLaunch) {
+        for (int64_t m0 = 0; m0 < M; m0 += kTokensPerLaunch) {
+            const int64_t mc = M - m0 < kTokensPerLaunch ? M - m0 : kTokensPerLaunch;
+            uint16_t* yc[st::kMaxProblems];
+            for (int i = 0; i < count; i++) yc[i] = ys[i] + m0 * Ns[i];
+            const cudaError_t e = launch_stream(x + m0 * K, count, codes, scales, yc, Ns, mc, K, num_sms, stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (M > 32) {  // wide tiles: one CTA per 128 rows x T tokens
         st::Params P = {};
         P.count = count;

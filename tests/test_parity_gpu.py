@@ -283,6 +283,31 @@ def test_linear_huge_k(nf4, o, m, n, k):
     assert ok, f"M={m} N={n} K={k}: worst ratio {ratio:.3f}"
 
 
+def test_linear_more_tokens_than_one_grid(nf4, o):
+    """M = 65535 * 256 + 40 tokens (more token tiles than the grid's y dimension holds), K = 64,
+    N = 24: the call runs in two chunks; 4096 sampled tokens, those around the chunk boundary and
+    the first and last included, checked against the oracle."""
+    from nf4_weight_only_gb300 import synth
+    chunk = 65535 * 256
+    m, n, k = chunk + 40, 24, 64
+    w = synth.device_weights(730, n, k, DEV)
+    codes, scales = nf4.quantize(w)
+    x = synth.device_activations_bf16(731, m, k, DEV)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    nf4.nf4_linear(x, codes, scales, y)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    c_ref, s_ref = o.quantize(w.cpu().numpy())
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    rng = np.random.default_rng(732)
+    toks = np.unique(np.concatenate([[0, m - 1, chunk - 2, chunk - 1, chunk, chunk + 1, chunk + 39],
+                                     rng.integers(0, m, 4089)]))
+    sel = torch.from_numpy(toks.astype(np.int64)).to(DEV)
+    y64, mag = o.linear(dev_to_bits(x[sel]), c_ref, s_ref, nthreads=16)
+    ok, ratio, mask = oracle.within_tolerance(dev_to_bits(y[sel]), y64, mag)
+    assert ok, f"{np.count_nonzero(~mask)} sampled outputs outside tolerance (worst {ratio:.3f})"
+
+
 def test_linear_five_million_rows(nf4, o):
     """N = 5,000,000 rows of K = 64 at M = 1 (the GEMV's row-range split over the whole grid);
     4096 sampled rows, the first and the last included, checked against the oracle."""
