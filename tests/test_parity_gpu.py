@@ -213,6 +213,93 @@ def test_linear_deterministic(nf4, o):
     assert np.array_equal(y1, y2)
 
 
+def _entry_point_calls(nf4):
+    """One call of every compute entry point (GEMV, both streaming kernels, grouped, quantize,
+    dequant, embed), inputs and outputs allocated up front; returns a function(stream)."""
+    from nf4_weight_only_gb300 import synth
+    w = synth.device_weights(800, 512, 2048, DEV)
+    codes = torch.empty((512, 1024), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((512, 32), dtype=torch.float16, device=DEV)
+    nf4.nf4_quantize(w, codes, scales)
+    w_hat = torch.empty((512, 2048), dtype=torch.bfloat16, device=DEV)
+    xs = {m: synth.device_activations_bf16(801 + m, m, 2048, DEV) for m in (1, 8, 300)}
+    ys = {m: torch.empty((m, 512), dtype=torch.bfloat16, device=DEV) for m in (1, 8, 300)}
+    g_ys = [torch.empty((8, 512), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    ids = torch.arange(0, 512, 7, dtype=torch.int32, device=DEV)
+    rows = torch.empty((ids.numel(), 2048), dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+
+    def calls(stream):
+        nf4.nf4_quantize(w, codes, scales, stream)
+        nf4.nf4_dequant(codes, scales, w_hat, stream)
+        for m in (1, 8, 300):
+            nf4.nf4_linear(xs[m], codes, scales, ys[m], stream)
+        nf4.nf4_linear_grouped(xs[8], [codes, codes], [scales, scales], g_ys, stream)
+        nf4.nf4_embed(ids, codes, scales, rows, stream)
+    return calls
+
+
+def test_calls_neither_sync_nor_allocate(nf4):
+    """After the first call on a device, no entry point waits for the device or allocates device
+    memory: queued behind a ~100 ms device sleep, every call returns to the host at once, and the
+    device's free memory is the same after 20 rounds of all of them."""
+    import time
+    calls = _entry_point_calls(nf4)
+    stream = torch.cuda.Stream(device=DEV)
+    calls(stream)  # first use per device: builds the constant table (one host wait, documented)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(DEV)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000_000)  # ~100 ms of device time ahead of the calls
+        t0 = time.perf_counter()
+        for _ in range(20):
+            calls(stream)
+        host_s = time.perf_counter() - t0
+    assert not stream.query(), "the sleep ended before the calls returned: the host waited"
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(DEV)
+    assert host_s < 0.05, f"140 calls took {host_s * 1e3:.1f} ms on the host (a synchronising call?)"
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    assert device_error(nf4) == 0
+
+
+_DETERMINISM_SCRIPT = r"""
+import hashlib, torch
+import nf4_weight_only_gb300 as nf4
+from nf4_weight_only_gb300 import synth
+nf4.load()
+dev = torch.device("cuda", 0)
+h = hashlib.sha256()
+for m, n, k, seed in [(1, 1000, 5120, 0), (3, 300, 11008, 1), (8, 2048, 6144, 2), (300, 777, 2048, 3)]:
+    codes, scales = nf4.quantize(synth.device_weights(810 + seed, n, k, dev))
+    x = synth.device_activations_bf16(820 + seed, m, k, dev)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    nf4.nf4_linear(x, codes, scales, y)
+    g = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    nf4.nf4_linear_grouped(x, [codes, codes], [scales, scales], g)
+    torch.cuda.synchronize()
+    for t in (codes, scales, y, g[0], g[1]):
+        h.update(t.cpu().view(torch.uint8).numpy().tobytes() if t.dtype == torch.uint8
+                 else t.cpu().view(torch.int16).numpy().tobytes())
+print("HASH", h.hexdigest())
+"""
+
+
+def test_outputs_identical_across_fresh_processes(nf4):
+    """The same inputs give the same output bytes in three fresh processes (GEMV, both streaming
+    kernels, grouped launches, quantize)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hashes = []
+    for _ in range(3):
+        r = subprocess.run([sys.executable, "-c", _DETERMINISM_SCRIPT], cwd=root, capture_output=True, text=True,
+                           timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        hashes.append([l for l in r.stdout.splitlines() if l.startswith("HASH ")][-1])
+    assert len(set(hashes)) == 1, hashes
+
+
 def test_concurrent_host_threads_and_streams(nf4, o):
     """Four host threads, each with its own stream, run the GEMV (M = 1, 3), the T <= 32 streaming
     kernel (M = 8), the wide one (M = 300) and a grouped launch ten times each, all at once: every
