@@ -561,6 +561,33 @@ def test_linear_grouped(nf4, o, m):
         assert ok, ratio
 
 
+@pytest.mark.parametrize("m", [1, 3, 8, 100])
+def test_linear_grouped_eight(nf4, o, m):
+    """The most linears one grouped call takes (8), ragged row counts with an empty one, K = 640
+    (ten groups, a ragged K-slice): GEMV (M = 1, 3), narrow (M = 8) and wide (M = 100) streaming;
+    every output meets the oracle bound."""
+    from nf4_weight_only_gb300 import synth
+    k = 640
+    ns = [1, 130, 0, 257, 64, 7, 1000, 3]
+    x = synth.activations_bf16(70 + m, m, k)
+    xd = bf16_to_dev(x)
+    mats = []
+    for i, n in enumerate(ns):
+        c, s = o.quantize(synth.weights(80 + i, n, k)) if n else (np.zeros((0, k // 2), np.uint8),
+                                                                  np.zeros((0, k // 64), np.uint16))
+        mats.append((c, s, torch.from_numpy(c).to(DEV), torch.from_numpy(s.view(np.int16)).view(torch.float16).to(DEV)))
+    ys = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for n in ns]
+    nf4.nf4_linear_grouped(xd, [t[2] for t in mats], [t[3] for t in mats], ys)
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    for (c, s, _, _), y, n in zip(mats, ys, ns):
+        if n == 0:
+            continue
+        y64, mag = o.linear(x, c, s, nthreads=16)
+        ok, ratio, _ = oracle.within_tolerance(dev_to_bits(y), y64, mag)
+        assert ok, f"N={n}: worst ratio {ratio:.3f}"
+
+
 # ------------------------------------------------------------------------------------------------
 # small-M tensor-core streaming (M <= 32): tiles of 128 rows plus a partial tile split into
 # K-slices, ragged last stages, every token-tile size
