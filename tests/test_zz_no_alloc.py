@@ -68,9 +68,13 @@ def test_two_calls_in_a_row_match_nf4_linear(nf4):
     for x, (_, _, ch, sh), y in zip(xs, mats, got):
         nf4.nf4_linear_host_noalloc(x, ch, sh, y)
     torch.cuda.synchronize()
+    # The oracle quantizes the generator's fp32 weights itself (the packed copies must match them)
+    # and bounds the outputs with its own codes and the generator's x.
     o = oracle.default()
-    for i, (x, (_, _, ch, sh), y) in enumerate(zip(xs, mats, got)):
-        y64, mag = o.linear(dev_to_bits(x), ch.numpy(), sh.view(torch.int16).numpy().view(np.uint16), nthreads=16)
+    for i, (x, (_, _, ch, sh), y, (_, n, k, seed)) in enumerate(zip(xs, mats, got, cases)):
+        c_ref, s_ref = o.quantize(synth.device_weights(seed, n, k, DEV).cpu().numpy())
+        assert np.array_equal(ch.numpy(), c_ref) and np.array_equal(sh.view(torch.int16).numpy().view(np.uint16), s_ref)
+        y64, mag = o.linear(dev_to_bits(x), c_ref, s_ref, nthreads=16)
         ok, ratio, _ = oracle.within_tolerance(dev_to_bits(y), y64, mag)
         assert ok, f"call {i}: outside the oracle bound, worst ratio {ratio:.3f}"
 
