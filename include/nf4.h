@@ -30,6 +30,14 @@
  *     M, N and K must each be at most 2^31 - 1.
  *   - Non-finite inputs are outside the contract: results are unspecified, but no call faults.
  *   - The same inputs give the same output bytes on every call (no atomics, fixed reduction order).
+ *   - The first linear call on a device builds a small constant table (one kernel and one wait on
+ *     `stream`).  Make that first call outside stream capture: under capture it returns
+ *     NF4_ERR_CAPTURE and touches neither the capture nor the stream.  Later calls may be captured.
+ *   - Every pipeline wait inside the kernels is bounded (one second of wall-clock time per wait by
+ *     default).  A wait that runs out records a code in the device error word, and the kernel
+ *     drains and exits instead of hanging; the call itself has already returned NF4_OK and the
+ *     outputs of that launch are then unspecified.  Callers that need to know read the word with
+ *     nf4_check_device_error (the tests and the benchmark do after every timed region).
  *   - Every entry point except the ring calls (see their section) may be called from several host
  *     threads at once, on the same or different streams: the only shared state is the per-device
  *     capability cache (atomic), one-time kernel attributes (std::call_once) and the per-device
@@ -47,7 +55,7 @@ extern "C" {
 #endif
 
 #define NF4_GROUP_SIZE 64
-#define NF4_ABI_VERSION 2
+#define NF4_ABI_VERSION 3
 
 typedef enum nf4_status {
     NF4_OK = 0,
@@ -57,8 +65,10 @@ typedef enum nf4_status {
     NF4_ERR_ALIAS = 4,              /* an output range overlaps an input range */
     NF4_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 (sm_103) */
     NF4_ERR_CUDA = 6,               /* a CUDA runtime call or kernel launch failed */
-    NF4_ERR_MEMORY = 7              /* memory of the wrong kind: a host pointer that is not page-locked,
+    NF4_ERR_MEMORY = 7,             /* memory of the wrong kind: a host pointer that is not page-locked,
                                        or a ring used on a device other than its own */
+    NF4_ERR_CAPTURE = 8             /* the first call on a device was made while `stream` is being captured
+                                       into a CUDA graph: its one-time set-up cannot run inside a capture */
 } nf4_status;
 
 /*
@@ -222,6 +232,8 @@ nf4_status nf4_ring_destroy(nf4_ring* ring);
  * between them) race on the array and give wrong results.
  * Set-up: the first call on a device looks up the array's device address (and, like the first
  * nf4_linear, builds the kernels' lookup table); make that first call before any stream capture.
+ * A first call made while `stream` is capturing returns NF4_ERR_CAPTURE and leaves the capture
+ * untouched.
  */
 #define NF4_NOALLOC_SLOT_BYTES (16 * 1024 * 1024)
 nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* codes, const uint16_t* scales, uint16_t* y,
@@ -229,11 +241,11 @@ nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* codes, cons
 
 /*
  * nf4_check_device_error - diagnostics: read and clear the device-side error words of the current
- * device.  The linear kernels bound every pipeline wait (about one second); a wait that runs out
- * records a nonzero code (1..39; 39 is nf4_diag_bounded_wait's), and the kernel drains and exits
- * instead of hanging.  nf4_embed
- * records 41 for an id outside the table.  *code receives the first recorded code (0 = none).
- * This call waits for the device (it is not meant for the hot path).
+ * device.  The linear kernels bound every pipeline wait (one second of wall-clock time per wait,
+ * see nf4_diag_set_wait_limit); a wait that runs out records a nonzero code (1..39; 39 is
+ * nf4_diag_bounded_wait's), and the kernel drains and exits instead of hanging, leaving its outputs
+ * unspecified.  nf4_embed records 41 for an id outside the table.  *code receives the first
+ * recorded code (0 = none).  This call waits for the device (it is not meant for the hot path).
  */
 nf4_status nf4_check_device_error(int* code);
 
@@ -241,17 +253,34 @@ nf4_status nf4_check_device_error(int* code);
  * nf4_diag_bounded_wait - diagnostics, no counterpart in the pages: checks that a pipeline wait
  * which runs out reports instead of hanging.  Launches one thread on `stream` that waits on an
  * mbarrier nothing ever arrives on, through the same bounded wait and error word as the linear
- * kernels; after `cycles` SM clocks it gives up and records code 39, which nf4_check_device_error
- * then returns.  The device stays usable.  cycles must be in [1, 2^31] (about one second at the
- * GB300's top clock), else NF4_ERR_SHAPE.
+ * kernels; after `ns` nanoseconds of wall-clock time it gives up and records code 39, which
+ * nf4_check_device_error then returns.  The device stays usable.  ns must be in [1, 2^31] (about
+ * 2.1 s), else NF4_ERR_SHAPE.
  */
-nf4_status nf4_diag_bounded_wait(int64_t cycles, cudaStream_t stream);
+nf4_status nf4_diag_bounded_wait(int64_t ns, cudaStream_t stream);
+
+/*
+ * nf4_diag_set_wait_limit - diagnostics, no counterpart in the pages: sets the wall-clock limit of
+ * each pipeline wait of the linear kernels on the current device to `ns` nanoseconds, or restores
+ * the default of one second when ns = 0.  The limit applies to every wait separately (it restarts
+ * at each wait), so a kernel that runs far longer than the limit is unaffected as long as each of
+ * its waits is shorter.  Stream-ordered on `stream`.  ns must be in [0, 2^36] (about 69 s), else
+ * NF4_ERR_SHAPE.
+ */
+nf4_status nf4_diag_set_wait_limit(int64_t ns, cudaStream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* nf4_status_str(nf4_status status);
 
 /* NF4_ABI_VERSION of the built library. */
 int nf4_abi_version(void);
+
+/* NF4_NOALLOC_SLOT_BYTES of the built library (the size of nf4_linear_host_noalloc's array). */
+int64_t nf4_noalloc_slot_bytes(void);
+
+/* Name of the last CUDA error (for instance "cudaErrorInvalidValue") behind an NF4_ERR_CUDA returned
+ * to the calling host thread, or "cudaSuccess" if there was none.  Static string, never NULL. */
+const char* nf4_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -19,12 +19,14 @@ GROUP = 64
 LIB_PATH = _build.LIB_PATH
 
 STATUS_NAMES = {0: "NF4_OK", 1: "NF4_ERR_NULL", 2: "NF4_ERR_SHAPE", 3: "NF4_ERR_ALIGN",
-                4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA", 7: "NF4_ERR_MEMORY"}
+                4: "NF4_ERR_ALIAS", 5: "NF4_ERR_UNSUPPORTED_DEVICE", 6: "NF4_ERR_CUDA", 7: "NF4_ERR_MEMORY",
+                8: "NF4_ERR_CAPTURE"}
 
 # Every symbol include/nf4.h declares.
 EXPORTED = ("nf4_quantize", "nf4_dequant", "nf4_linear", "nf4_linear_grouped", "nf4_embed",
             "nf4_ring_create", "nf4_ring_run", "nf4_ring_destroy", "nf4_linear_host_noalloc",
-            "nf4_check_device_error", "nf4_diag_bounded_wait", "nf4_status_str", "nf4_abi_version")
+            "nf4_check_device_error", "nf4_diag_bounded_wait", "nf4_diag_set_wait_limit", "nf4_status_str",
+            "nf4_abi_version", "nf4_noalloc_slot_bytes", "nf4_last_cuda_error")
 
 
 class HostLinear(ctypes.Structure):
@@ -77,6 +79,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nf4_check_device_error.restype = ci
     lib.nf4_diag_bounded_wait.argtypes = [i64, vp]
     lib.nf4_diag_bounded_wait.restype = ci
+    lib.nf4_diag_set_wait_limit.argtypes = [i64, vp]
+    lib.nf4_diag_set_wait_limit.restype = ci
+    lib.nf4_noalloc_slot_bytes.argtypes = []
+    lib.nf4_noalloc_slot_bytes.restype = i64
+    lib.nf4_last_cuda_error.argtypes = []
+    lib.nf4_last_cuda_error.restype = ctypes.c_char_p
     lib.nf4_abi_version.argtypes = []
     lib.nf4_abi_version.restype = ci
     if path is None:
@@ -107,6 +115,8 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
 
 def _check(status: int, what: str) -> None:
     if status != 0:
+        if status == 6:  # NF4_ERR_CUDA: name the CUDA error behind it
+            raise NF4Error(status, f"{what} [{load().nf4_last_cuda_error().decode()}]")
         raise NF4Error(status, what)
 
 
@@ -202,23 +212,30 @@ class Ring:
         self.close()
 
 
-NOALLOC_SLOT_BYTES = 16 * 1024 * 1024  # NF4_NOALLOC_SLOT_BYTES
+def noalloc_slot_bytes() -> int:
+    """Size of nf4_linear_host_noalloc's static device array, as the built library reports it."""
+    return int(load().nf4_noalloc_slot_bytes())
 
 
 def nf4_linear_host_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
                             stream=None) -> None:
     """y[M, N] = x[M, K] * w_hat^T with codes [N, K/2] and scales [N, K/64] in pinned host memory,
-    staged through the library's static device buffer (no allocation; at most NOALLOC_SLOT_BYTES)."""
+    staged through the library's static device buffer (no allocation; at most noalloc_slot_bytes())."""
     m, k = x.shape
     n = codes.shape[0]
     _check(load().nf4_linear_host_noalloc(_ptr(x), _ptr(codes), _ptr(scales), _ptr(y), m, n, k, _stream(stream)),
            "nf4_linear_host_noalloc")
 
 
-def nf4_diag_bounded_wait(cycles: int, stream=None) -> None:
-    """Launch one thread whose bounded wait on a barrier nothing arrives on runs out after `cycles`
-    SM clocks and records code 39 in the device error word (diagnostics)."""
-    _check(load().nf4_diag_bounded_wait(int(cycles), _stream(stream)), "nf4_diag_bounded_wait")
+def nf4_diag_bounded_wait(ns: int, stream=None) -> None:
+    """Launch one thread whose bounded wait on a barrier nothing arrives on runs out after `ns`
+    nanoseconds and records code 39 in the device error word (diagnostics)."""
+    _check(load().nf4_diag_bounded_wait(int(ns), _stream(stream)), "nf4_diag_bounded_wait")
+
+
+def nf4_diag_set_wait_limit(ns: int, stream=None) -> None:
+    """Set the per-wait wall-clock limit of the kernels' pipeline waits (ns = 0 restores 1 s)."""
+    _check(load().nf4_diag_set_wait_limit(int(ns), _stream(stream)), "nf4_diag_set_wait_limit")
 
 
 def nf4_check_device_error() -> int:

@@ -14,6 +14,9 @@ int64_t gemv_max_k(int64_t M);
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// The last CUDA error this host thread saw inside the library (read by nf4_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
 
 // Per-device cache: 0 = unknown, -1 = unsupported, otherwise the SM count of a 10.3 device.
@@ -35,7 +38,7 @@ nf4_status check_k(int64_t K) {
 // Current device must be compute capability 10.3; returns its SM count through `sms`.
 nf4_status current_device(int* device, int* sms) {
     if (cudaGetDevice(device) != cudaSuccess) {
-        cudaGetLastError();
+        g_last_cuda_error = cudaGetLastError();
         return NF4_ERR_CUDA;
     }
     if (*device < 0 || *device >= kMaxDevices) return NF4_ERR_UNSUPPORTED_DEVICE;
@@ -45,7 +48,7 @@ nf4_status current_device(int* device, int* sms) {
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *device) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *device) != cudaSuccess ||
             cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess) {
-            cudaGetLastError();
+            g_last_cuda_error = cudaGetLastError();
             return NF4_ERR_CUDA;
         }
         cached = (major == 10 && minor == 3 && count > 0) ? count : -1;
@@ -58,14 +61,23 @@ nf4_status current_device(int* device, int* sms) {
 
 nf4_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return NF4_OK;
+    g_last_cuda_error = e;
     cudaGetLastError();
     return NF4_ERR_CUDA;
+}
+
+// ensure_tables reports a first call under stream capture as cudaErrorStreamCaptureUnsupported.
+nf4_status from_tables(cudaError_t e) {
+    return e == cudaErrorStreamCaptureUnsupported ? NF4_ERR_CAPTURE : from_cuda(e);
 }
 
 }  // namespace
 
 namespace nf4 {
 int abi_current_device(int* device, int* sms) { return current_device(device, sms); }
+void note_cuda_error(cudaError_t e) {
+    if (e != cudaSuccess) g_last_cuda_error = e;
+}
 }  // namespace nf4
 
 extern "C" {
@@ -80,11 +92,15 @@ const char* nf4_status_str(nf4_status status) {
         case NF4_ERR_UNSUPPORTED_DEVICE: return "NF4_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
         case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA call or launch failed";
         case NF4_ERR_MEMORY: return "NF4_ERR_MEMORY: host memory not page-locked, or a ring used on another device";
+        case NF4_ERR_CAPTURE:
+            return "NF4_ERR_CAPTURE: first call on this device made under stream capture (make one call outside capture first)";
     }
     return "NF4 status: unknown code";
 }
 
 int nf4_abi_version(void) { return NF4_ABI_VERSION; }
+
+const char* nf4_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count, const uint8_t* const* codes,
                               const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns,
@@ -122,7 +138,7 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
     }
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
-    if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
+    if ((st = from_tables(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
     // drop empty problems, keep the order
     const uint8_t* c[nf4::kMaxGroupedLinears];
     const uint16_t* sc[nf4::kMaxGroupedLinears];
@@ -155,12 +171,20 @@ nf4_status nf4_check_device_error(int* code) {
     return NF4_OK;
 }
 
-nf4_status nf4_diag_bounded_wait(int64_t cycles, cudaStream_t stream) {
-    if (cycles <= 0 || cycles > (int64_t{1} << 31)) return NF4_ERR_SHAPE;
+nf4_status nf4_diag_bounded_wait(int64_t ns, cudaStream_t stream) {
+    if (ns <= 0 || ns > (int64_t{1} << 31)) return NF4_ERR_SHAPE;
     int dev = 0, sms = 0;
     nf4_status st = current_device(&dev, &sms);
     if (st != NF4_OK) return st;
-    return from_cuda(nf4::launch_diag_wait(cycles, stream));
+    return from_cuda(nf4::launch_diag_wait(ns, stream));
+}
+
+nf4_status nf4_diag_set_wait_limit(int64_t ns, cudaStream_t stream) {
+    if (ns < 0 || ns > (int64_t{1} << 36)) return NF4_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    nf4_status st = current_device(&dev, &sms);
+    if (st != NF4_OK) return st;
+    return from_cuda(nf4::set_wait_limit(ns, stream));
 }
 
 nf4_status nf4_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
@@ -222,7 +246,7 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     if (overlap(y, yb, x, xb) || overlap(y, yb, codes, cb) || overlap(y, yb, scales, sb)) return NF4_ERR_ALIAS;
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
-    if ((st = from_cuda(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
+    if ((st = from_tables(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
     if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
         return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
     return from_cuda(nf4::launch_stream(x, 1, &codes, &scales, &y, &N, M, K, sms, stream));

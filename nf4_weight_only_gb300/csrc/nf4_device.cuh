@@ -164,12 +164,35 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait on phase `parity`; false once `deadline` (clock64) has passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long deadline) {
+
+// Wall-clock time in nanoseconds (the GPU's global timer; the same on every SM).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on phase `parity`: true once the phase has completed, false if it has not completed
+// `limit_ns` nanoseconds of wall-clock time after this wait began.  Every wait gets its own limit
+// (a long kernel with many short waits never runs out), and the timer is read only when the first
+// test fails.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
     while (!mbar_test(bar, parity)) {
-        if (clock64() > deadline) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// One lane of a converged warp (the same lane on every call) is true.  tcgen05.mma, tcgen05.commit
+// and the TMA copies are issued by a single thread, but the warp around it runs the issue loop in
+// step: its operands then stay warp-uniform, which lets each instruction issue in tens of cycles
+// instead of hundreds (measured on this GPU).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float f) {

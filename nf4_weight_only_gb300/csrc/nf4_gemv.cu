@@ -44,22 +44,31 @@ constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 // out in blocks of eight: the eight low-byte chunks, then the eight high-byte chunks, so the chunk
 // of row m sits at index m + (m & ~7) (+ 8 for the high bytes) and eight lanes reading random rows
 // spread over all eight 16-byte bank groups of a 128-byte line.
-__device__ uint4 g_vtab[2048];
+// Rows 0..1023 hold V[m][c] = bf16(fp32(T[c] * (1 + m/1024))); rows 1024..2047 hold 2 * V[m][c] (the
+// same values one binade up, exact); row 2048 is all zeros.  The GEMV reads rows 0..1023 (the first
+// 2048 chunks); the small-M streaming kernel reads all of them.
+constexpr int kVtabRows = 2049;
+constexpr int kVtabChunks = 2 * 2048 + 16;  // chunk index of row 2048's high bytes is 4104
+__device__ uint4 g_vtab[kVtabChunks];
 
 __global__ void build_vtab_kernel() {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;  // mantissa class of the scale
-    if (m >= 1024) return;
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= kVtabRows) return;
+    const int m = row & 1023;  // mantissa class of the scale
     const float s1 = __uint_as_float(0x3F800000u | (static_cast<uint32_t>(m) << 13));  // 1 + m/1024
     uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+    if (row < 2048) {
 #pragma unroll
-    for (int c = 0; c < 16; c++) {
-        const uint32_t b = bf16_bits(__fmul_rn(kNF4[c], s1));
-        const int slot = c < 8 ? c : 8 + (15 - c);  // byte position inside the 16-byte plane
-        lo[slot >> 2] |= (b & 0xFFu) << (8 * (slot & 3));
-        hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
+        for (int c = 0; c < 16; c++) {
+            uint32_t b = bf16_bits(__fmul_rn(kNF4[c], s1));
+            if (row >= 1024) b = bf16_bits(2.0f * __uint_as_float(b << 16));  // exact: one binade up
+            const int slot = c < 8 ? c : 8 + (15 - c);  // byte position inside the 16-byte plane
+            lo[slot >> 2] |= (b & 0xFFu) << (8 * (slot & 3));
+            hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
+        }
     }
-    g_vtab[m + (m & ~7)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    g_vtab[m + (m & ~7) + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    g_vtab[row + (row & ~7)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    g_vtab[row + (row & ~7) + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
 // Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order.
@@ -129,7 +138,9 @@ __device__ __forceinline__ int problem_of(const GemvProblems& P, int64_t r) {
 __device__ int g_tc_error;
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_tc_error, 0, code); }
 
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz: a wait this long means a bug
+// Wall-clock limit of one pipeline wait, in nanoseconds (1 s by default: a wait that long means a
+// bug, not a slow GPU).  Every wait has its own limit, so no kernel length can exhaust it.
+__device__ unsigned long long g_wait_ns = 1000000000ull;
 
 // Per-row metadata the producer writes next to each row's data.
 struct RowMeta {
@@ -199,14 +210,14 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const long long deadline = clock64() + kWaitCycles;
+    const uint64_t wait_ns = g_wait_ns;
 
     if (warp == C + 1) {
         // ------------------------------------------------------------------ reducer
         constexpr int LPV = 32 / V;  // lanes holding one value after the halving steps
         int st = 0, par = 0;
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, deadline))) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, wait_ns))) {
                 record_error(13);
                 break;
             }
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         // 16-byte copies.  Every row of the block gets its metadata (valid = 0 past the end).
         int st = 0, round = 0;  // ring stage of block t and how often the ring has wrapped
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, round += st == 0) {
-            if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (L.ST + st), (round - 1) & 1, deadline))) {
+            if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (L.ST + st), (round - 1) & 1, wait_ns))) {
                 record_error(11);
                 break;
             }
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         asm volatile("bar.sync 1, %0;" ::"r"(32 * C) : "memory");  // every consumer's table chunks landed
         int st = 0, par = 0;  // ring stage of block t and the phase parity of its barriers
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, deadline))) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, wait_ns))) {
                 record_error(12);
                 break;
             }
@@ -474,9 +485,34 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
 }  // namespace nf4
 
 #include "nf4_stream.cuh"
+#include "nf4_narrow.cuh"
 
 namespace nf4 {
 namespace {
+
+// cuTensorMapEncodeTiled is a driver call and needs a current context.  A host thread whose first
+// CUDA work in this library is a tensor-map encode may not have one yet: the runtime binds the
+// primary context to a thread lazily, at its first call that needs it.  Bind it here when the thread
+// has no context at all (a context the caller made current is left alone).
+cudaError_t ensure_current_context() {
+    static PFN_cuCtxGetCurrent_v4000 get = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        else
+            cudaGetLastError();
+    });
+    CUcontext c = nullptr;
+    if (get && get(&c) == CUDA_SUCCESS && c != nullptr) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaSetDevice(dev);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -505,6 +541,7 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     using C = st::Cfg<T>;
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
+    if (const cudaError_t e = ensure_current_context(); e != cudaSuccess) return e;
     // x: bf16 [M][K] viewed as [M][G][64]; a box is T tokens x S consecutive groups x 64, which lands
     // as pseudo-token rows t * S + s of 128 bytes (128-byte swizzle).  Groups past G and tokens past M
     // read as zero.
@@ -539,19 +576,31 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const size_t smem = C::kBytes + 1024;  // + slack to align the base to 1024 bytes
+    // T <= 32: the small-M kernel (nf4_narrow.cuh); wider tiles: the GEMM form (nf4_stream.cuh)
+    uint32_t kBytes;
+    int kThreads;
+    void (*kernel)(const CUtensorMap, const CUtensorMap, const st::CodeMaps, const st::Params);
+    if constexpr (T <= 32) {
+        kBytes = st::NCfg<T>::kBytes;
+        kThreads = st::NCfg<T>::kThreads;
+        kernel = st::narrow_kernel<T>;
+    } else {
+        kBytes = C::kBytes;
+        kThreads = C::kThreads;
+        kernel = st::stream_kernel<T>;
+    }
+    const size_t smem = kBytes + 1024;  // + slack to align the base to 1024 bytes
     static std::once_flag attr_once[64];
     int dev = 0;
     cudaGetDevice(&dev);
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(st::stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
+        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(P.cta0[P.count]), static_cast<unsigned>((M + T - 1) / T));
-    cfg.blockDim = dim3(C::kThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -559,7 +608,7 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, st::stream_kernel<T>, maps[0], maps[1], cm, P);
+    return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], cm, P);
 }
 
 }  // namespace
@@ -671,20 +720,27 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
 }
 
 // One thread waits on an mbarrier that nothing arrives on, with the pipelines' bounded wait and
-// error word: after `cycles` SM clocks the wait gives up and records 39 (the check of a timed-out
+// error word: after `ns` nanoseconds the wait gives up and records 39 (the check of a timed-out
 // wait's reporting path; no fault, no hang).
-__global__ void diag_wait_kernel(long long cycles) {
+__global__ void diag_wait_kernel(uint64_t ns) {
     __shared__ __align__(8) unsigned long long bar;
     if (threadIdx.x != 0) return;
     const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
     mbar_init(b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (!mbar_wait(b, 0, clock64() + cycles)) record_error(39);
+    if (!mbar_wait(b, 0, ns)) record_error(39);
 }
 
-cudaError_t launch_diag_wait(int64_t cycles, cudaStream_t stream) {
-    diag_wait_kernel<<<1, 32, 0, stream>>>(static_cast<long long>(cycles));
+cudaError_t launch_diag_wait(int64_t ns, cudaStream_t stream) {
+    diag_wait_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(ns));
     return cudaGetLastError();
+}
+
+// Sets the per-wait limit of every pipeline wait on the current device (ns > 0), or restores the
+// default of one second (ns = 0).  Stream-ordered after the work already on `stream`.
+cudaError_t set_wait_limit(int64_t ns, cudaStream_t stream) {
+    const unsigned long long v = ns > 0 ? static_cast<unsigned long long>(ns) : 1000000000ull;
+    return cudaMemcpyToSymbolAsync(g_wait_ns, &v, sizeof(v), 0, cudaMemcpyHostToDevice, stream);
 }
 
 cudaError_t read_and_clear_error(int* code) {
@@ -705,7 +761,14 @@ cudaError_t ensure_tables(int device, cudaStream_t stream) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_tables.mu);
     if (g_tables.ready[device]) return cudaSuccess;
-    build_vtab_kernel<<<4, 256, 0, stream>>>();
+    // The build waits for `stream`, which a capture forbids: refuse before touching it.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorStreamCaptureUnsupported;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
+    build_vtab_kernel<<<(kVtabRows + 255) / 256, 256, 0, stream>>>();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // One-time wait so that later calls on any stream see the table.

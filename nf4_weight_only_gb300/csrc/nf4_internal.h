@@ -30,17 +30,23 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
                           cudaStream_t stream);
 // Device error word of the linear kernels (nonzero after a bounded pipeline wait timed out).
 cudaError_t read_and_clear_error(int* code);
-cudaError_t launch_diag_wait(int64_t cycles, cudaStream_t stream);
+cudaError_t launch_diag_wait(int64_t ns, cudaStream_t stream);
+// Per-wait wall-clock limit of the pipeline waits on the current device (0 = the default, 1 s).
+cudaError_t set_wait_limit(int64_t ns, cudaStream_t stream);
 
 // Packed embedding rows (out-of-range ids write zeros and set the embed error word to 41).
 cudaError_t launch_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes, const uint16_t* scales, int64_t V,
                          int64_t K, uint16_t* out, int num_sms, cudaStream_t stream);
 cudaError_t read_and_clear_embed_error(int* code);
 
-// Per-device constant table used by the GEMV (built once per device, stream-ordered).
+// Per-device constant table used by the linear kernels (built once per device with one wait on
+// `stream`).  Returns cudaErrorStreamCaptureUnsupported, touching nothing, when the table is not
+// built yet and `stream` is being captured.
 cudaError_t ensure_tables(int device, cudaStream_t stream);
 
 // The C-ABI layer's device check (an nf4_status value): the current device and its SM count.
 int abi_current_device(int* device, int* sms);
+// Records a CUDA error for nf4_last_cuda_error (no-op for cudaSuccess).
+void note_cuda_error(cudaError_t e);
 
 }  // namespace nf4

@@ -1,0 +1,484 @@
+// Small-M NF4 weight streaming (decode and prefill up to 32 positions) on the tcgen05 tensor cores,
+// sm_103a: y[M, N] = x[M, K] * w_hat[N, K]^T for 1 <= M <= 32.
+//
+// The deep-fold README's execution-path table runs the N = 1 decode GEMV and the prefill GEMM of up
+// to 32 positions over packed weights, dequantizing only the current tile.  These shapes are bound
+// by the weight stream and by the integer work of the exact 16-entry lookups, so every
+// multiply-add goes to the tensor cores and the CUDA cores run the lookups alone:
+//
+//   dequant warps:  packed codes (shared memory) -> exact bf16 w_hat -> tensor memory (tcgen05.st)
+//   MMA warp:       tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
+//                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
+//
+// K-slices (as in nf4_stream.cuh).  A CTA owns a contiguous range of output rows, processed as tiles
+// of R rows; the 128 MMA rows of a tile are R rows x S K-slices (R * S <= 128): MMA row r * S + s
+// holds row r's groups s, S + s, 2S + s, ...  The B tile holds, for token t and slice s, the x values
+// of group kb*S + s as pseudo-token column t * S + s, and the epilogue adds the S partials of each
+// (row, token) in slice order.  A CTA with a dozen rows still fills all 128 MMA rows, so the grid is
+// one CTA per SM with a balanced row range each.
+//
+// Pipeline stage = 128 k per MMA row (two 64-k sub-stages, 8 MMAs of K = 16).  Stage q uses A slot
+// q mod NA in tensor memory and x slot q mod NA in shared memory (both sub-tiles of the stage), so
+// one tcgen05.commit per stage frees both.  The MMA warp waits twice per stage (x landed, A written)
+// and commits once; it runs converged and one elected lane issues (see elect_one).
+//
+// Exponent folding.  A nonzero scale is 2^E * (1 + m/1024) with E = 2q + p, p in {0, 1}.  The table
+// row 1024 p + m holds 2^p * V[m][c] = bf16(T[c] * 2^p * (1 + m/1024)) exactly (rounding commutes
+// with powers of two), and 2^(2q) is added to every entry by adding q to its high byte (the
+// exponent's bits 7..1): four IMADs per group, no ALU work.  A zero scale reads the all-zero row.  A
+// negative scale (never produced by nf4_quantize, but allowed) flips the sign bits of the nonzero
+// entries on a warp-uniform branch.
+//
+// Warp roles: warp 0 streams codes (TMA) and scale windows, warp 1 owns tensor memory and issues the
+// MMAs, warps 2 .. 4*kSets+1 are kSets sets of four dequant warps (a set takes every kSets-th stage;
+// the four warps of a set cover the four 32-lane quarters of tensor memory) that also run the
+// epilogue of every kSets-th tile, and the last warp streams x.  Weights do not depend on the
+// previous kernel in the stream, so warp 0 never waits for it; only x and y do.
+// Every mbarrier wait is bounded (wall clock, per wait); a wait that runs out records an error code,
+// the roles drain the copies and MMAs in flight (bounded again) and tensor memory is always freed.
+#pragma once
+
+namespace nf4 {
+namespace st {
+
+template <int T>
+struct NCfg {
+    static constexpr int kJMax = T == 1 ? 16 : (T <= 4 ? 32 : 64);  // columns of B and of each D
+    static constexpr int kSMax = kJMax / T < 8 ? kJMax / T : 8;        // K-slices per tile
+    static constexpr int kAccN = 4;                                    // K-step k8 -> accumulator k8 % 4
+    static constexpr int kDCols = kAccN * kJMax;
+    static constexpr int kAStages = ((512 - kDCols) / 64 < 8 ? (512 - kDCols) / 64 : 8) & ~1;
+    static constexpr int kSets = 3;
+    static constexpr int kXWarp = 2 + 4 * kSets;
+    static constexpr int kThreads = 32 * (kXWarp + 1);
+    static constexpr int kLoadStages = T >= 16 ? 3 : 4;
+    static constexpr int kScaleStages = 3;
+    static constexpr uint32_t kXSub = kJMax * 128;  // one 64-k x sub-tile (multiple of 1024 bytes)
+    static constexpr uint32_t kXSlot = 2 * kXSub;
+    static constexpr uint32_t kVtabBytes = kVtabChunks * 16;
+    static constexpr uint32_t kOffCodes = kAStages * kXSlot;
+    static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
+    static constexpr uint32_t kOffScales = kOffVtab + kVtabBytes;
+    static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
+    static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
+    static constexpr uint32_t kBytes = kOffBars + 1024;
+    static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
+    static_assert(kDCols + 64 * kAStages <= 512, "tensor memory budget");
+    static_assert(8 * (2 * kLoadStages + 3 * kAStages + 2 * kScaleStages + 2 * kSets + 2) + 4 <= 1024, "barrier area");
+};
+
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane, without waiting for the store.
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+template <int T>
+__global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
+    narrow_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
+                  const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
+    using C = NCfg<T>;
+    constexpr int NA = C::kAStages, NL = C::kLoadStages, NSS = C::kScaleStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = P.G;
+
+    // barriers
+    const uint32_t b_lfull = sbase + C::kOffBars;   // [NL] codes load stage landed (tx)
+    const uint32_t b_lempty = b_lfull + 8 * NL;     // [NL] codes load stage read (weighted releases)
+    const uint32_t b_xfull = b_lempty + 8 * NL;     // [NA] x slot landed (tx)
+    const uint32_t b_afull = b_xfull + 8 * NA;      // [NA] A slot written (4 warps)
+    const uint32_t b_empty = b_afull + 8 * NA;      // [NA] A and x slot read by the MMAs (commit)
+    const uint32_t b_sfull = b_empty + 8 * NA;      // [NSS] scale tile landed (32 producer lanes)
+    const uint32_t b_sempty = b_sfull + 8 * NSS;    // [NSS] scale tile read (weighted releases)
+    const uint32_t b_dfull = b_sempty + 8 * NSS;    // [kSets] accumulators complete (commit), per epilogue set
+    const uint32_t b_ep = b_dfull + 8 * C::kSets;   // [kSets] per-set epilogue rendezvous
+    const uint32_t b_dfree = b_ep + 8 * C::kSets;   // accumulators read (4 warps)
+    const uint32_t b_mdone = b_dfree + 8;           // every MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * NL + 3 * NA + 2 * NSS + 2 * C::kSets + 2));
+
+    // this CTA's problem and rows
+    int p = 0;
+    for (int i = 1; i < P.count; i++)
+        if (static_cast<int>(blockIdx.x) >= P.cta0[i]) p = i;
+    const int rbeg = (static_cast<int>(blockIdx.x) - P.cta0[p]) * P.rstar;
+    const int rows_cta = P.n[p] - rbeg < P.rstar ? P.n[p] - rbeg : P.rstar;
+    const int ntiles = rows_cta / 128 + (rows_cta % 128 != 0);
+    const int m0 = static_cast<int>(blockIdx.y) * T;  // first token of this CTA
+
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NL; i++) {
+            mbar_init(b_lfull + 8 * i, 1);
+            mbar_init(b_lempty + 8 * i, 8);  // weighted releases of the stages that read it
+        }
+        for (int i = 0; i < NA; i++) {
+            mbar_init(b_xfull + 8 * i, 1);
+            mbar_init(b_afull + 8 * i, 4);
+            mbar_init(b_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < NSS; i++) {
+            mbar_init(b_sfull + 8 * i, 32);
+            mbar_init(b_sempty + 8 * i, 48);
+        }
+        for (int i = 0; i < C::kSets; i++) {
+            mbar_init(b_dfull + 8 * i, 1);
+            mbar_init(b_ep + 8 * i, 4);
+        }
+        mbar_init(b_dfree, 4);
+        mbar_init(b_mdone, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < kVtabChunks; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
+    cp_async_commit();
+    cp_async_wait<0>();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t wait_ns = g_wait_ns;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- codes and scales
+        // Lane 0 issues the TMA boxes (elected, converged warp); the warp copies scale windows.
+        const uint8_t* sbytes = reinterpret_cast<const uint8_t*>(P.scales[p]);
+        const int64_t s_total = static_cast<int64_t>(P.n[p]) * G * 2;
+        const CUtensorMap* cm_full = &cmaps.full[p];
+        const CUtensorMap* cm_rem = &cmaps.rem[p];
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_full)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(cm_rem)) : "memory");
+        }
+        __syncwarp();
+        bool ok = true;
+        int lq = 0, lslot = 0, lround = 0, sslot = 0, sround = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int U = load_span(t.s);
+            const CUtensorMap* cmap = t.s > 1 ? cm_rem : cm_full;
+            const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;  // all boxes of a stage
+            const int BS = box_span(t.s);
+            const uint32_t per_row = (t.s + 2) * 16;
+            for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
+                if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
+                    if (lround > 0 && !warp_wait(b_lempty + 8 * lslot, (lround - 1) & 1, wait_ns)) {
+                        if (lane == 0) record_error(21);
+                        ok = false;
+                        break;
+                    }
+                    expect_tx_elect(b_lfull + 8 * lslot, cbytes);
+                    for (int b = 0; b < U / BS; b++)
+                        tma_load_2d_elect(sbase + C::kOffCodes + lslot * kLoadBytes + b * kBoxStride, cmap,
+                                          (g + b * BS * t.s) * 32, t.row0, b_lfull + 8 * lslot);
+                    lq++;
+                    if (++lslot == NL) {
+                        lslot = 0;
+                        lround++;
+                    }
+                }
+                if ((kb & 7) == 0) {  // scale tile: groups g .. g + 8S - 1 of every row
+                    if (sround > 0 && !warp_wait(b_sempty + 8 * sslot, (sround - 1) & 1, wait_ns)) {
+                        if (lane == 0) record_error(22);
+                        ok = false;
+                        break;
+                    }
+                    const int g1 = g + 8 * t.s < G ? g + 8 * t.s : G;
+                    uint8_t* dst = smem + C::kOffScales + sslot * kScaleSlot;
+                    for (int r = lane; r < t.rows; r += 32) {
+                        const int64_t rb = static_cast<int64_t>(t.row0 + r) * G * 2;
+                        const int64_t a = (rb + 2 * g) & ~static_cast<int64_t>(15);
+                        for (int64_t c = a; c < rb + 2 * g1; c += 16) {
+                            const int64_t left = s_total - c;
+                            cp_async16(dst + r * per_row + (c - a), sbytes + c, static_cast<uint32_t>(left < 16 ? left : 16));
+                        }
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_sfull + 8 * sslot)
+                                 : "memory");
+                    if (++sslot == NSS) {
+                        sslot = 0;
+                        sround++;
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        cp_async_wait<0>();
+        // drain: the codes of the last ring round have landed before the CTA may exit
+        for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, kDrainNs);
+    } else if (warp == C::kXWarp) {
+        // ---------------------------------------------------------------- x
+        // Stage q's two 64-k sub-tiles land in x slot q mod NA, counted on that slot's own barrier.
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
+        }
+        __syncwarp();
+        pdl_wait();  // x may be written by the previous grid in the stream
+        bool ok = true;
+        int q = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
+            const uint32_t subbytes = 128u * t.s * T;
+            for (int kb2 = 0; kb2 < t.nt / 2; kb2++, q++) {
+                const int slot = q % NA, round = q / NA;
+                if (round > 0 && !warp_wait(b_empty + 8 * slot, (round - 1) & 1, wait_ns)) {
+                    if (lane == 0) record_error(23);
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = sbase + slot * C::kXSlot;
+                expect_tx_elect(b_xfull + 8 * slot, 2 * subbytes);
+                tma_load_3d_elect(dst, xmap, 0, 2 * kb2 * t.s, m0, b_xfull + 8 * slot);
+                tma_load_3d_elect(dst + C::kXSub, xmap, 0, (2 * kb2 + 1) * t.s, m0, b_xfull + 8 * slot);
+            }
+        }
+        // drain: the x slots of the last ring round have landed before the CTA may exit
+        for (int qq = q - NA > 0 ? q - NA : 0; qq < q; qq++) mbar_wait(b_xfull + 8 * (qq % NA), (qq / NA) & 1, kDrainNs);
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop (every operand warp-uniform); one elected lane issues.
+        bool ok = true;
+        int q = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int nmma = (T * t.s + 15) & ~15;
+            const uint32_t idesc = idesc_n(nmma < 16 ? 16 : nmma);
+            if (j > 0 && !warp_wait(b_dfree, (j - 1) & 1, wait_ns)) {
+                if (lane == 0) record_error(24);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kb2 = 0; kb2 < t.nt / 2; kb2++, q++) {
+                const int slot = q % NA;
+                const uint32_t par = (q / NA) & 1;
+                if (!warp_wait(b_xfull + 8 * slot, par, wait_ns) || !warp_wait(b_afull + 8 * slot, par, wait_ns)) {
+                    if (lane == 0) record_error(25);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_tmem = tmem_base + C::kDCols + 64 * slot;
+                const uint64_t bdesc = smem_desc_sw128(sbase + slot * C::kXSlot);
+#pragma unroll
+                for (int k8 = 0; k8 < 8; k8++) {  // K = 16 per MMA: 8 columns of A, 32 bytes of a B row
+                    const uint64_t b = bdesc + (k8 >= 4 ? (C::kXSub >> 4) : 0) + 2 * (k8 & 3);
+                    mma_tmem_a_elect(tmem_base + (k8 % C::kAccN) * C::kJMax, a_tmem + 8 * k8, b, idesc,
+                                     kb2 > 0 || k8 >= C::kAccN);
+                }
+                mma_commit_elect(b_empty + 8 * slot);
+            }
+            if (ok) mma_commit_elect(b_dfull + 8 * (j % C::kSets));
+        }
+        mma_commit_elect(b_mdone);  // the CTA exits only after every MMA it issued has completed
+        mbar_wait(b_mdone, 0, kDrainNs);
+    } else {
+        // ---------------------------------------------------------------- dequant + epilogue
+        const int set = (warp - 2) >> 2;
+        const int quarter = warp & 3;             // tensor-memory lanes this warp may access
+        const int i = quarter * 32 + lane;        // MMA row
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint4* vtab = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
+        bool ok = true;
+        int ep_uses = 0;
+        // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
+        // ring slots and phases follow from them, so a set visits only its own stages.
+        int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
+        // A warp waits only for the codes load stage and the scale tile of its own stages, and its
+        // set releases them after use; the release counts are weighted so that a slot completes when
+        // every stage that reads it is done (a load stage: 8 = two stages of four warps, or one at
+        // weight 2; a scale tile: 48 = n stages of four warps at weight 12 / n).  A parity wait is
+        // sound when the slot's previous fill has completed and its next cannot have: the next
+        // needs this warp's own release, and the previous is complete once the fills are at most
+        // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
+        // A set's stages are kSets apart; a load stage holds two stages (S = 1) or one, a scale tile
+        // four.  The A slot of a stage is reused NA stages later; a set's previous stage (kSets
+        // earlier) waited for the slot of kSets + NA stages back, so with NA >= kSets the wait for
+        // the slot's previous use (NA back) is on a phase whose predecessor has completed.
+        static_assert(C::kSets <= NL && C::kSets <= NA && NSS >= 2, "ring too shallow for the release rule");
+        for (int j = 0; j < ntiles && ok; j++) {
+            q0 += nst_prev;
+            l0 += nload_prev;
+            s0 += nscale_prev;
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int U = load_span(t.s), BS = box_span(t.s);
+            const int lbs = BS == 4 ? 2 : (BS == 2 ? 1 : 0);  // log2 BS
+            const int nst = t.nt / 2, nload = (t.nt + U - 1) / U, nscale = (t.nt + 7) / 8;
+            nst_prev = nst;
+            nload_prev = nload;
+            nscale_prev = nscale;
+            const int r = i / t.s, sl = i - (i / t.s) * t.s;
+            const bool lane_ok = r < t.rows;
+            const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
+            // codes of row r in a box: rowb bytes, 16-byte chunks permuted by the 128-byte swizzle
+            // (chunk ^ (r mod 8)) when the row is 128 bytes
+            const uint32_t rowb = 32u * BS * t.s;
+            const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
+            const uint8_t* crow0 = smem + C::kOffCodes + r * rowb;
+            // this lane's scale inside a scale tile: row r's window starts at the 16-byte boundary
+            // below its first scale; sub-stage kb adds 2 * (kb mod 8) * S bytes
+            const uint8_t* srow0 = smem + C::kOffScales +
+                                   (r * (t.s + 2) * 16 + static_cast<uint32_t>((static_cast<int64_t>(t.row0 + r) * G * 2) & 15) + 2 * sl);
+            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets)
+            for (int kb2 = (set - q0 % C::kSets + C::kSets) % C::kSets; kb2 < nst && ok; kb2 += C::kSets) {
+                const int gq = q0 + kb2;
+                const int aslot = gq % NA, around = gq / NA;
+                const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
+                const int li = kbs / U;                   // its codes load stage, tile-relative
+                const int si = kbs >> 3;                  // its scale tile, tile-relative
+                const int L = l0 + li, S = s0 + si;       // CTA-wide
+                const int lslot = L % NL, sslot = S % NSS;
+                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, wait_ns) &&
+                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, wait_ns);
+                if (good && around > 0) good = warp_wait(b_empty + 8 * aslot, (around - 1) & 1, wait_ns);
+                if (!good) {
+                    if (lane == 0) record_error(26);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (warp_ok) {
+#pragma unroll 1
+                    for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
+                        const int kb = kbs + h;
+                        const int u = kb & (U - 1);  // sub-stage in the load stage: box u / BS
+                        uint32_t out[32];
+                        const int g = kb * t.s + sl;
+                        if (lane_ok && g < G) {
+                            const uint8_t* crow = crow0 + lslot * kLoadBytes + (u >> lbs) * kBoxStride;
+                            const uint32_t ch = static_cast<uint32_t>(((u & (BS - 1)) * t.s + sl) * 2);
+                            const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
+                            const uint16_t sc = *reinterpret_cast<const uint16_t*>(srow0 + sslot * kScaleSlot + 2 * (kb & 7) * t.s);
+                            // scale = sign * 2^(2q + p) * (1 + m/1024): row 1024 p + m of the table, q
+                            // added to the high byte of every nonzero entry (code 7's byte stays 0)
+                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
+                            const uint32_t mag = sb & 0x7FFFFFFFu;
+                            const uint32_t nz = mag != 0u ? 1u : 0u;
+                            const uint32_t e = mag >> 23;
+                            const uint32_t pbit = (e & 1u) ^ 1u;                       // (e - 127) mod 2
+                            const int q = (static_cast<int>(e) - 127 - static_cast<int>(pbit)) >> 1;
+                            const uint32_t row = nz ? ((mag >> 13) & 0x3FFu) + (pbit << 10) : 2048u;
+                            const uint32_t qq = static_cast<uint32_t>(q) * nz;
+                            uint4 tl = vtab[row + (row & ~7u)];
+                            uint4 th = vtab[row + (row & ~7u) + 8];
+                            th.x += qq * 0x01010101u;
+                            th.y += qq * 0x00010101u;
+                            th.z += qq * 0x01010101u;
+                            th.w += qq * 0x01010101u;
+                            if (__any_sync(__activemask(), (sb >> 31) != 0u)) {  // a negative scale (rare)
+                                const uint32_t sg = ((sb >> 31) != 0u && nz) ? 0x80808080u : 0u;
+                                th.x ^= sg;
+                                th.y ^= sg & 0x00FFFFFFu;
+                                th.z ^= sg;
+                                th.w ^= sg;
+                            }
+                            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                            for (int w = 0; w < 8; w++) {
+                                uint32_t o4[4];
+                                lookup8(words[w], tl, th, P.m1, P.p16, o4);
+                                out[4 * w + 0] = o4[0];
+                                out[4 * w + 1] = o4[1];
+                                out[4 * w + 2] = o4[2];
+                                out[4 * w + 3] = o4[3];
+                            }
+                        } else {
+#pragma unroll
+                            for (int w = 0; w < 32; w++) out[w] = 0u;
+                        }
+                        tmem_st32_nowait(tmem_base + lane_addr + C::kDCols + 64 * aslot + 32 * h, out);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b_afull + 8 * aslot);
+                    const int touching = U == 4 ? (nst - 2 * li < 2 ? nst - 2 * li : 2) : 1;
+                    mbar_arrive_count(b_lempty + 8 * lslot, 2 / touching);
+                    const int stouch = nst - 4 * si < 4 ? nst - 4 * si : 4;
+                    mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
+                }
+            }
+            if (!ok || j % C::kSets != set) continue;
+            // ------------------------------------------------------------ epilogue of tile j
+            if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, wait_ns)) {
+                if (lane == 0) record_error(26);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            pdl_wait();  // y may still be read by the previous grid (returns at once by now)
+            const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
+            uint16_t* y = P.y[p];
+            float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+            const int J = T * t.s;
+            for (int c = 0; c < J; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + lane_addr + c, v);
+#pragma unroll
+                for (int a = 1; a < C::kAccN; a++) {  // add the accumulators in order
+                    uint32_t w[16];
+                    tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++) v[cc] = __float_as_uint(__uint_as_float(v[cc]) + __uint_as_float(w[cc]));
+                }
+#pragma unroll
+                for (int cc = 0; cc < 16; cc++) {
+                    const int col = c + cc;
+                    if (t.s == 1) {
+                        if (lane_ok && col < M)
+                            y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
+                    } else {
+                        const int rel = col - sl;
+                        const int tt = rel / t.s;
+                        if (rel >= 0 && rel == tt * t.s && tt < M) red[tt * 128 + i] = __uint_as_float(v[cc]);
+                    }
+                }
+            }
+            if (C::kSMax > 1 && t.s > 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_ep + 8 * set);
+                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
+                    if (lane == 0) record_error(27);
+                    ok = false;
+                    break;
+                }
+                ep_uses++;
+                for (int o = i; o < t.rows * M; o += 128) {
+                    const int tt = o / t.rows, rr = o - tt * t.rows;
+                    float acc = 0.0f;
+                    for (int s2 = 0; s2 < t.s; s2++) acc += red[tt * 128 + rr * t.s + s2];
+                    y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = bf16_bits(acc);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dfree);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
+    }
+}
+
+}  // namespace st
+}  // namespace nf4

@@ -147,7 +147,7 @@ nf4_status nf4_ring_run(nf4_ring* r, const nf4_host_linear* ops, int64_t count, 
     std::lock_guard<std::mutex> lock(r->mu);
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
-        cudaGetLastError();
+        nf4::note_cuda_error(cudaGetLastError());
         return NF4_ERR_CUDA;
     }
     const bool capturing = cap == cudaStreamCaptureStatusActive;
@@ -158,7 +158,7 @@ nf4_status nf4_ring_run(nf4_ring* r, const nf4_host_linear* ops, int64_t count, 
     r->captured = r->captured || capturing;
     if (r->captured && (cudaEventRecord(r->fork, stream) != cudaSuccess ||
                       cudaStreamWaitEvent(r->copy, r->fork, 0) != cudaSuccess)) {
-        cudaGetLastError();
+        nf4::note_cuda_error(cudaGetLastError());
         return NF4_ERR_CUDA;
     }
     bool recorded_here[2] = {false, false};
@@ -178,12 +178,12 @@ nf4_status nf4_ring_run(nf4_ring* r, const nf4_host_linear* ops, int64_t count, 
                   cudaEventRecord(r->filled[s], r->copy) == cudaSuccess &&
                   cudaStreamWaitEvent(stream, r->filled[s], 0) == cudaSuccess;
         if (!ok) {
-            cudaGetLastError();
+            nf4::note_cuda_error(cudaGetLastError());
             return NF4_ERR_CUDA;
         }
         if ((st = nf4_linear(op.x, codes, scales, op.y, op.M, op.N, op.K, stream)) != NF4_OK) return st;
         if (cudaEventRecord(r->consumed[s], stream) != cudaSuccess) {
-            cudaGetLastError();
+            nf4::note_cuda_error(cudaGetLastError());
             return NF4_ERR_CUDA;
         }
         recorded_here[s] = true;
@@ -222,11 +222,12 @@ constexpr int kMaxSlotDevices = 64;
 std::mutex g_noalloc_mu;
 uint8_t* g_noalloc_ptr[kMaxSlotDevices] = {};
 
-// Device address of g_noalloc_slot on `device` (the current device); nullptr on failure.
-uint8_t* noalloc_slot(int device) {
+// Device address of g_noalloc_slot on `device` (the current device), looked up on the first call;
+// nullptr on failure.  With `lookup` false it only returns an address found before (or nullptr).
+uint8_t* noalloc_slot(int device, bool lookup) {
     if (device < 0 || device >= kMaxSlotDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[device]) {
+    if (!g_noalloc_ptr[device] && lookup) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_slot) != cudaSuccess || !p) {
             cudaGetLastError();
@@ -246,15 +247,28 @@ extern "C" nf4_status nf4_linear_host_noalloc(const uint16_t* x, const uint8_t* 
     if (st != NF4_OK || M == 0 || N == 0) return st;
     int dev = 0, sms = 0;
     if ((st = static_cast<nf4_status>(nf4::abi_current_device(&dev, &sms))) != NF4_OK) return st;
-    uint8_t* slot = noalloc_slot(dev);
-    if (!slot) return NF4_ERR_CUDA;
+    uint8_t* slot = noalloc_slot(dev, false);
+    if (!slot) {
+        // First call on this device: the address lookup may load the library's device code, which a
+        // capture forbids, so refuse under capture before touching anything.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return NF4_ERR_CAPTURE;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return NF4_ERR_CAPTURE;
+        slot = noalloc_slot(dev, true);
+        if (!slot) return NF4_ERR_CUDA;
+    }
     uint16_t* slot_scales = reinterpret_cast<uint16_t*>(slot + scales_offset(op));
     if (cudaMemcpyAsync(slot, codes, static_cast<size_t>(codes_bytes(op)), cudaMemcpyHostToDevice, stream) !=
             cudaSuccess ||
         cudaMemcpyAsync(slot_scales, scales, static_cast<size_t>(scales_bytes(op)), cudaMemcpyHostToDevice, stream) !=
             cudaSuccess) {
-        cudaGetLastError();
+        nf4::note_cuda_error(cudaGetLastError());
         return NF4_ERR_CUDA;
     }
     return nf4_linear(x, slot, slot_scales, y, M, N, K, stream);
 }
+
+extern "C" int64_t nf4_noalloc_slot_bytes(void) { return NF4_NOALLOC_SLOT_BYTES; }

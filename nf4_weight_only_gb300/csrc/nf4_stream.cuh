@@ -47,20 +47,13 @@
 
 #include <cuda.h>
 
-#ifndef KSETS_WIDE
-#define KSETS_WIDE 4
-#endif
-#ifndef KSETS_NARROW
-#define KSETS_NARROW 3
-#endif
-
 namespace nf4 {
 namespace st {
 
 constexpr uint32_t kScaleSlot = 6144;           // R * (S + 2) 16-byte chunks with R * S <= 128
 constexpr uint32_t kLoadBytes = 16384;          // one codes load stage: <= 128 MMA rows x 128 bytes
 constexpr int kMaxProblems = 8;
-constexpr long long kDrainCycles = 200000000LL;
+constexpr uint64_t kDrainNs = 100000000ull;  // limit of each wait while draining after a timeout (0.1 s)
 
 // Four accumulators: K-step ks of every stage goes to accumulator ks, so that no MMA waits for the
 // previous one to finish (with N of 16..64 an MMA is short); the epilogue adds the four in order.
@@ -74,7 +67,7 @@ struct Cfg {
     static constexpr int kAccN = kWide ? 1 : kAcc;                    // accumulators
     // dequant warp sets (four warps each, one per 32-lane quarter of tensor memory); a set takes
     // every kSets-th stage, so more sets hide more of the lookups' latency
-    static constexpr int kSets = kWide ? KSETS_WIDE : KSETS_NARROW;
+    static constexpr int kSets = kWide ? 4 : 3;
     static constexpr int kXWarp = 2 + 4 * kSets;      // the x producer, after the dequant warps
     static constexpr int kThreads = 32 * (kXWarp + 1);
     static constexpr int kTmemCols = 512;
@@ -151,13 +144,6 @@ __device__ __forceinline__ Tile tile_of(const Params& P, int rbeg, int rows_cta,
     return t;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -170,12 +156,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     d |= static_cast<uint64_t>(1) << 46;                   // descriptor version for tcgen05
     d |= static_cast<uint64_t>(2) << 61;                   // swizzle mode: 128 bytes
     return d;
-}
-
-// Arrives on `bar` once every tcgen05.mma this thread issued before has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
 }
 
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane.
@@ -202,22 +182,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
+
+
+// D[128 x N] (+)= A[128 x 16] * B[N x 16]^T with A read from tensor memory, issued by one elected
+// lane of a converged warp (all 32 lanes execute the call with the same operands; see elect_one).
+__device__ __forceinline__ void mma_tmem_a_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
-
-// D[128 x N] (+)= A[128 x 16] * B[N x 16]^T with A read from tensor memory.
-__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                           uint32_t acc) {
+// Arrives on `bar` once every tcgen05.mma issued before by this warp's elected lane has completed.
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+// Arm `bar` for `bytes` of transaction and start one 2D / 3D TMA box into `dst`, from one elected
+// lane of a converged warp.
+__device__ __forceinline__ void expect_tx_elect(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n\t}"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                  uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n\t}"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 
@@ -240,16 +244,10 @@ __device__ __forceinline__ uint32_t idesc_n(int n) {
 }
 
 // Bounded wait by all 32 lanes (warp-uniform result).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long deadline) {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, deadline));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, limit_ns));
 }
 
-// Bounded wait by lane 0 alone, result broadcast to the warp.
-__device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, long long deadline, int lane) {
-    bool w = true;
-    if (lane == 0) w = mbar_wait(bar, parity, deadline);
-    return __shfl_sync(0xFFFFFFFFu, w, 0);
-}
 
 template <int T>
 __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
@@ -329,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const long long deadline = clock64() + kWaitCycles;
+    const uint64_t wait_ns = g_wait_ns;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
@@ -355,17 +353,15 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const uint32_t per_row = (t.s + 2) * 16;
             for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
                 if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
-                    if (lround > 0 && !lane0_wait(b_lempty + 8 * lslot, (lround - 1) & 1, deadline, lane)) {
+                    if (lround > 0 && !warp_wait(b_lempty + 8 * lslot, (lround - 1) & 1, wait_ns)) {
                         if (lane == 0) record_error(21);
                         ok = false;
                         break;
                     }
-                    if (lane == 0) {
-                        mbar_expect_tx(b_lfull + 8 * lslot, cbytes);
-                        for (int b = 0; b < U / BS; b++)
-                            tma_load_2d(sbase + C::kOffCodes + lslot * kLoadBytes + b * kBoxStride, cmap,
-                                        (g + b * BS * t.s) * 32, t.row0, b_lfull + 8 * lslot);
-                    }
+                    expect_tx_elect(b_lfull + 8 * lslot, cbytes);
+                    for (int b = 0; b < U / BS; b++)
+                        tma_load_2d_elect(sbase + C::kOffCodes + lslot * kLoadBytes + b * kBoxStride, cmap,
+                                          (g + b * BS * t.s) * 32, t.row0, b_lfull + 8 * lslot);
                     lq++;
                     if (++lslot == NL) {
                         lslot = 0;
@@ -373,7 +369,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     }
                 }
                 if ((kb & 7) == 0) {  // scale tile: groups g .. g + 8S - 1 of every row
-                    if (sround > 0 && !warp_wait(b_sempty + 8 * sslot, (sround - 1) & 1, deadline)) {
+                    if (sround > 0 && !warp_wait(b_sempty + 8 * sslot, (sround - 1) & 1, wait_ns)) {
                         if (lane == 0) record_error(22);
                         ok = false;
                         break;
@@ -401,95 +397,97 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         cp_async_wait<0>();
         // drain: the codes of the last ring round have landed before the CTA may exit
         if (lane == 0) {
-            const long long dl = clock64() + kDrainCycles;
+            const uint64_t dl = kDrainNs;
             for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, dl);
         }
     } else if (warp == C::kXWarp) {
         // ---------------------------------------------------------------- x producer
+        // The whole warp runs the loop; one elected lane issues each TMA box (warp-uniform operands).
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
-            pdl_wait();  // x may be written by the previous grid in the stream
-            bool ok = true;
-            int kq = 0, xslot = 0, xround = 0;
-            for (int j = 0; j < ntiles && ok; j++) {
-                const Tile t = tile_of(P, rbeg, rows_cta, j);
-                const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
-                const uint32_t xbytes = 128u * t.s * T;
-                for (int g = 0; g < t.nt * t.s; g += t.s) {  // a sub-stage: groups g .. g + S - 1
-                    if (xround > 0 && !mbar_wait(b_xempty + 8 * xslot, (xround - 1) & 1, deadline)) {
-                        record_error(23);
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(b_xfull + 8 * xslot, xbytes);
-                    tma_load_3d(sbase + xslot * C::kXBytes, xmap, 0, g, m0, b_xfull + 8 * xslot);
-                    kq++;
-                    if (++xslot == NX) {
-                        xslot = 0;
-                        xround++;
-                    }
-                }
-            }
-            // drain: the x tiles of the last ring round have landed before the CTA may exit
-            const long long dl = clock64() + kDrainCycles;
-            for (int qq = kq - NX > 0 ? kq - NX : 0; qq < kq; qq++) mbar_wait(b_xfull + 8 * (qq % NX), (qq / NX) & 1, dl);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            bool ok = true;
-            int aslot = 0, xslot = 0;
-            uint32_t aph = 0, xph = 0;
-            for (int j = 0; j < ntiles && ok; j++) {
-                const Tile t = tile_of(P, rbeg, rows_cta, j);
-                const int nmma = (T * t.s + 15) & ~15;
-                const uint32_t idesc = idesc_n(nmma < 16 ? 16 : nmma);
-                if (j > 0 && !mbar_wait(b_dfree, (j - 1) & 1, deadline)) {
-                    record_error(24);
+        __syncwarp();
+        pdl_wait();  // x may be written by the previous grid in the stream
+        bool ok = true;
+        int kq = 0, xslot = 0, xround = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
+            const uint32_t xbytes = 128u * t.s * T;
+            for (int g = 0; g < t.nt * t.s; g += t.s) {  // a sub-stage: groups g .. g + S - 1
+                if (xround > 0 && !warp_wait(b_xempty + 8 * xslot, (xround - 1) & 1, wait_ns)) {
+                    if (lane == 0) record_error(23);
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                for (int kb = 0; kb < t.nt / 2 && ok; kb++) {
-                    if (!mbar_wait(b_afull + 8 * aslot, aph, deadline)) {
-                        record_error(25);
+                expect_tx_elect(b_xfull + 8 * xslot, xbytes);
+                tma_load_3d_elect(sbase + xslot * C::kXBytes, xmap, 0, g, m0, b_xfull + 8 * xslot);
+                kq++;
+                if (++xslot == NX) {
+                    xslot = 0;
+                    xround++;
+                }
+            }
+        }
+        // drain: the x tiles of the last ring round have landed before the CTA may exit
+        for (int qq = kq - NX > 0 ? kq - NX : 0; qq < kq; qq++) mbar_wait(b_xfull + 8 * (qq % NX), (qq / NX) & 1, kDrainNs);
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop, so that every operand stays warp-uniform, and one elected
+        // lane issues each tcgen05.mma and tcgen05.commit (a single diverged lane issuing them took
+        // several times longer per instruction on this GPU).
+        bool ok = true;
+        int aslot = 0, xslot = 0;
+        uint32_t aph = 0, xph = 0;
+        for (int j = 0; j < ntiles && ok; j++) {
+            const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int nmma = (T * t.s + 15) & ~15;
+            const uint32_t idesc = idesc_n(nmma < 16 ? 16 : nmma);
+            if (j > 0 && !warp_wait(b_dfree, (j - 1) & 1, wait_ns)) {
+                if (lane == 0) record_error(24);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kb = 0; kb < t.nt / 2 && ok; kb++) {
+                if (!warp_wait(b_afull + 8 * aslot, aph, wait_ns)) {
+                    if (lane == 0) record_error(25);
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_tmem = tmem_base + C::kDCols + 64 * aslot;
+                for (int h = 0; h < 2; h++) {  // two 64-k sub-stages, each with its own x sub-tile
+                    if (!warp_wait(b_xfull + 8 * xslot, xph, wait_ns)) {
+                        if (lane == 0) record_error(25);
                         ok = false;
                         break;
                     }
-                    const uint32_t a_tmem = tmem_base + C::kDCols + 64 * aslot;
-                    for (int h = 0; h < 2; h++) {  // two 64-k sub-stages, each with its own x sub-tile
-                        if (!mbar_wait(b_xfull + 8 * xslot, xph, deadline)) {
-                            record_error(25);
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t bdesc = smem_desc_sw128(sbase + xslot * C::kXBytes);
+                    tc_fence_after();
+                    const uint64_t bdesc = smem_desc_sw128(sbase + xslot * C::kXBytes);
 #pragma unroll
-                        for (int ks = 0; ks < 4; ks++) {  // K = 16 per MMA: 8 columns of A, 32 bytes of B
-                            const int k8 = 4 * h + ks;
-                            mma_tmem_a(tmem_base + (k8 % C::kAccN) * C::kJMax, a_tmem + 8 * k8, bdesc + 2 * ks, idesc,
-                                       kb > 0 || k8 >= C::kAccN);
-                        }
-                        mma_commit(b_xempty + 8 * xslot);
-                        if (++xslot == NX) {
-                            xslot = 0;
-                            xph ^= 1;
-                        }
+                    for (int ks = 0; ks < 4; ks++) {  // K = 16 per MMA: 8 columns of A, 32 bytes of B
+                        const int k8 = 4 * h + ks;
+                        mma_tmem_a_elect(tmem_base + (k8 % C::kAccN) * C::kJMax, a_tmem + 8 * k8, bdesc + 2 * ks,
+                                         idesc, kb > 0 || k8 >= C::kAccN);
                     }
-                    if (!ok) break;
-                    mma_commit(b_aempty + 8 * aslot);
-                    if (++aslot == NA) {
-                        aslot = 0;
-                        aph ^= 1;
+                    mma_commit_elect(b_xempty + 8 * xslot);
+                    if (++xslot == NX) {
+                        xslot = 0;
+                        xph ^= 1;
                     }
                 }
-                if (ok) mma_commit(b_dfull + 8 * (j % C::kSets));
+                if (!ok) break;
+                mma_commit_elect(b_aempty + 8 * aslot);
+                if (++aslot == NA) {
+                    aslot = 0;
+                    aph ^= 1;
+                }
             }
-            mma_commit(b_mdone);  // the CTA exits only after every MMA it issued has completed
-            mbar_wait(b_mdone, 0, clock64() + kDrainCycles);
+            if (ok) mma_commit_elect(b_dfull + 8 * (j % C::kSets));
         }
+        mma_commit_elect(b_mdone);  // the CTA exits only after every MMA it issued has completed
+        mbar_wait(b_mdone, 0, kDrainNs);
     } else {
         // ---------------------------------------------------------------- dequant + epilogue (warps 2 .. kXWarp-1)
         const int set = (warp - 2) >> 2;
@@ -544,9 +542,9 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 const int si = kbs / 8;                   // its scale tile, tile-relative
                 const int L = l0 + li, S = s0 + si;       // CTA-wide
                 const int lslot = L % NL, sslot = S % NSS;
-                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, deadline) &&
-                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, deadline);
-                if (good && around > 0) good = warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, deadline);
+                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, wait_ns) &&
+                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, wait_ns);
+                if (good && around > 0) good = warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, wait_ns);
                 if (!good) {
                     record_error(26);
                     ok = false;
@@ -618,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             }
             if (!ok || j % C::kSets != set) continue;
             // ------------------------------------------------------------ epilogue of tile j
-            if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, deadline)) {
+            if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, wait_ns)) {
                 record_error(26);
                 ok = false;
                 break;
@@ -640,7 +638,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_ep + 8 * set);
-                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, deadline)) {
+                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
                     record_error(27);
                     ok = false;
                     break;
@@ -691,7 +689,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             if (C::kSMax > 1 && t.s > 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_ep + 8 * set);
-                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, deadline)) {
+                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
                     record_error(27);
                     ok = false;
                     break;
@@ -701,7 +699,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     const int tt = o / t.rows, rr = o - tt * t.rows;
                     float acc = 0.0f;
                     for (int s2 = 0; s2 < t.s; s2++) acc += red[tt * 128 + rr * t.s + s2];
-                    y[static_cast<int64_t>(tt) * np + t.row0 + rr] = bf16_bits(acc);
+                    y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = bf16_bits(acc);
                 }
             }
             tc_fence_before();

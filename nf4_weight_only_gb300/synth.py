@@ -56,3 +56,17 @@ def device_activations_bf16(seed: int, m: int, k: int, device) -> torch.Tensor:
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     return torch.randn((m, k), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def device_packed(seed: int, n: int, k: int, device, scale_lo: float = 0.01, scale_hi: float = 0.1):
+    """Random packed weights drawn on ``device``: uint8 code bytes [n, k/2], uniform over all 256
+    values, and fp16 scales [n, k/64], uniform in [scale_lo, scale_hi) rounded by torch's cast.
+
+    For runs too large to quantize from fp32 weights (tens of GB); a test that checks such a linear
+    copies the rows it checks back to the host, so both sides see identical bytes.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    codes = torch.randint(0, 256, (n, k // 2), generator=g, device=device, dtype=torch.uint8)
+    scales = (torch.rand((n, k // 64), generator=g, device=device) * (scale_hi - scale_lo) + scale_lo).to(torch.float16)
+    return codes, scales

@@ -34,8 +34,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.nf4_abi_version() == 2
-    for code in range(8):
+    assert lib.nf4_abi_version() == 3
+    for code in range(9):
         s = lib.nf4_status_str(code).decode()
         assert s.startswith("NF4_")
     assert b"unknown" in lib.nf4_status_str(99)
@@ -104,10 +104,24 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
 
 
 def test_diag_wait_rejects_unbounded_limits(lib):
-    """The diagnostic wait takes a limit in [1, 2^31] SM clocks; anything else is rejected on the host."""
+    """The diagnostic wait takes a limit in [1, 2^31] ns and the wait-limit setter one in [0, 2^36] ns;
+    anything else is rejected on the host."""
     lib.nf4_diag_bounded_wait.argtypes = [ctypes.c_int64, vp]
-    for cycles in (0, -1, (1 << 31) + 1, 1 << 62):
-        assert lib.nf4_diag_bounded_wait(cycles, None) == 2  # NF4_ERR_SHAPE
+    for ns in (0, -1, (1 << 31) + 1, 1 << 62):
+        assert lib.nf4_diag_bounded_wait(ns, None) == 2  # NF4_ERR_SHAPE
+    lib.nf4_diag_set_wait_limit.argtypes = [ctypes.c_int64, vp]
+    for ns in (-1, (1 << 36) + 1, 1 << 62):
+        assert lib.nf4_diag_set_wait_limit(ns, None) == 2
+
+
+def test_noalloc_size_matches_header(lib):
+    """The binding reads the no-alloc array's size from the library, which must equal the header's."""
+    text = open(os.path.join(ROOT, "include", "nf4.h")).read()
+    m = re.search(r"#define NF4_NOALLOC_SLOT_BYTES \((\d+) \* (\d+) \* (\d+)\)", text)
+    assert m, "NF4_NOALLOC_SLOT_BYTES not found in include/nf4.h"
+    want = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+    import nf4_weight_only_gb300 as nf4
+    assert nf4.noalloc_slot_bytes() == want
 
 
 def test_binding_raises_without_library(tmp_path):

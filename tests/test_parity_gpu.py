@@ -300,6 +300,37 @@ def test_outputs_identical_across_fresh_processes(nf4):
     assert len(set(hashes)) == 1, hashes
 
 
+def test_first_call_of_a_fresh_host_thread(nf4, o):
+    """A host thread whose first CUDA work is a library call on the tensor-core paths (M = 8 and
+    M = 300; their launch encodes tensor maps through the driver, which needs a current context)
+    gets the same bytes as the main thread."""
+    import threading
+    from nf4_weight_only_gb300 import synth
+    cases = []
+    for m, n, k, seed in [(8, 640, 2048, 0), (300, 384, 1024, 1)]:
+        codes, scales = nf4.quantize(synth.device_weights(960 + seed, n, k, DEV))
+        x = synth.device_activations_bf16(961 + seed, m, k, DEV)
+        ref = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+        nf4.nf4_linear(x, codes, scales, ref)
+        cases.append((x, codes, scales, ref, torch.empty_like(ref)))
+    torch.cuda.synchronize()
+    for x, codes, scales, ref, out in cases:
+        errors = []
+
+        def worker():
+            try:
+                nf4.nf4_linear(x, codes, scales, out)  # the thread's first CUDA call
+            except Exception as e:  # reported below
+                errors.append(repr(e))
+
+        th = threading.Thread(target=worker)
+        th.start()
+        th.join()
+        assert not errors, errors
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
 def test_concurrent_host_threads_and_streams(nf4, o):
     """Four host threads, each with its own stream, run the GEMV (M = 1, 3), the T <= 32 streaming
     kernel (M = 8), the wide one (M = 300) and a grouped launch ten times each, all at once: every
@@ -418,15 +449,56 @@ def test_linear_five_million_rows(nf4, o):
 
 
 def test_timed_out_wait_reports_and_device_stays_usable(nf4, o):
-    """A bounded wait that runs out (one thread on a barrier nothing arrives on, about 1 ms) records
+    """A bounded wait that runs out (one thread on a barrier nothing arrives on, 1 ms) records
     code 39 instead of hanging; the next linear on the same device is still correct."""
-    nf4.nf4_diag_bounded_wait(2_000_000)
+    nf4.nf4_diag_bounded_wait(1_000_000)
     torch.cuda.synchronize()
     assert device_error(nf4) == 39
     assert device_error(nf4) == 0  # reading clears the word
     check_linear(nf4, o, 1, 257, 2048, seed=5)
     check_linear(nf4, o, 8, 130, 192, seed=6)
     assert device_error(nf4) == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 16384, 786432), (1, 393216, 32768), (512, 16384, 131072)])
+def test_wait_limit_restarts_at_each_wait(nf4, o, m, n, k):
+    """Every pipeline wait limited to 100 us: a healthy linear that runs for more than ten times as
+    long (the streaming kernel at M = 1 with K = 786432, the GEMV over 393216 rows, the M = 512
+    GEMM; 6.8 GB or 2.2 TFLOP each) finishes with the device error word at 0 and correct sampled
+    rows, because the limit restarts at each wait.  Under the same limit the diagnostic wait still
+    reports code 39."""
+    from nf4_weight_only_gb300 import synth
+    codes, scales = synth.device_packed(740 + m, n, k, DEV)
+    x = synth.device_activations_bf16(741 + m, m, k, DEV)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    nf4.nf4_linear(x, codes, scales, y)  # first launch of the kernel (module load) outside the timing
+    torch.cuda.synchronize()
+    assert device_error(nf4) == 0
+    nf4.nf4_diag_set_wait_limit(100_000)
+    try:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        nf4.nf4_linear(x, codes, scales, y)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        assert device_error(nf4) == 0
+        assert ms > 1.0, f"the linear took {ms:.3f} ms, not long enough against the 0.1 ms limit"
+        nf4.nf4_diag_bounded_wait(1_000_000)
+        torch.cuda.synchronize()
+        assert device_error(nf4) == 39
+    finally:
+        nf4.nf4_diag_set_wait_limit(0)
+        torch.cuda.synchronize()
+    rng = np.random.default_rng(742)
+    rows = np.unique(np.concatenate([[0, 1, n // 2, n - 1], rng.integers(0, n, 4)]))
+    sel = torch.from_numpy(rows.astype(np.int64)).to(DEV)
+    y64, mag = o.linear(dev_to_bits(x), codes[sel].cpu().numpy(), f16_dev_to_bits(scales[sel]), nthreads=16)
+    ok, ratio, mask = oracle.within_tolerance(dev_to_bits(y)[:, rows], y64, mag)
+    assert ok, f"{np.count_nonzero(~mask)} sampled outputs outside tolerance (worst {ratio:.3f})"
+    del codes, scales, x, y
+    torch.cuda.empty_cache()
 
 
 def test_empty_is_noop(nf4):

@@ -51,7 +51,7 @@ def test_two_calls_in_a_row_match_nf4_linear(nf4):
     mats = [_weights(nf4, seed, n, k) for _, n, k, seed in cases]
     xs = [synth.device_activations_bf16(seed + 1, m, k, DEV) for m, _, k, seed in cases]
     for (_, n, k, _) in cases:
-        assert nf4.Ring.bytes_needed(n, k) <= nf4.NOALLOC_SLOT_BYTES
+        assert nf4.Ring.bytes_needed(n, k) <= nf4.noalloc_slot_bytes()
     want = [_resident(nf4, x, cd, sd) for x, (cd, sd, _, _) in zip(xs, mats)]
     got = [torch.full_like(w, 3.0) for w in want]
     stream = torch.cuda.Stream(device=DEV)
@@ -83,7 +83,7 @@ def test_refusals_leave_y_untouched(nf4):
     from nf4_weight_only_gb300 import synth
     # 16384 x 2048: 17.8 MB of packed weights, more than the 16 MiB array
     n, k = 16384, 2048
-    assert nf4.Ring.bytes_needed(n, k) > nf4.NOALLOC_SLOT_BYTES
+    assert nf4.Ring.bytes_needed(n, k) > nf4.noalloc_slot_bytes()
     _, _, ch, sh = _weights(nf4, 720, n, k)
     x = synth.device_activations_bf16(721, 1, k, DEV)
     y = torch.full((1, n), 5.0, dtype=torch.bfloat16, device=DEV)
