@@ -153,14 +153,14 @@ __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// Tests phase `parity` of `bar`; if it has not completed, the warp may sleep (up to ~0.5 ms) until it
-// does instead of spinning, which leaves the issue slots and the ALU pipe to the warps that work.
+// Tests phase `parity` of `bar` (the hardware may hold the thread up to the hint, 1 us, while the
+// phase is incomplete).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(500000u)
+        : "r"(bar), "r"(parity), "r"(1000u)
         : "memory");
     return ok != 0;
 }
@@ -174,15 +174,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Bounded wait on phase `parity`: true once the phase has completed, false if it has not completed
 // `limit_ns` nanoseconds of wall-clock time after this wait began.  Every wait gets its own limit
-// (a long kernel with many short waits never runs out), and the timer is read only when the first
-// test fails.
+// (a long kernel with many short waits never runs out).  The first test costs no timer read; after
+// that the waiting warp sleeps between tests (32 ns doubling to 256 ns), so warps that wait leave
+// the issue slots and the integer pipe to the warps that work, and it reads the timer only every
+// eighth test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return false;
+    uint32_t sleep_ns = 32;
+    for (uint32_t n = 1;; n++) {
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 256) sleep_ns *= 2;
+        if (mbar_test(bar, parity)) return true;
+        if ((n & 7) == 0 && global_ns() - t0 > limit_ns) return false;
     }
-    return true;
 }
 
 // One lane of a converged warp (the same lane on every call) is true.  tcgen05.mma, tcgen05.commit

@@ -38,17 +38,16 @@ constexpr int kHalfWarps = 8;  // consumer warps of a CTA that leaves room for a
 constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
 constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
 
-// V table: row m holds the low bytes {L(0..3), L(4..7), L(15..12), L(11..8)} and the high bytes in
-// the same order, L / H being the low / high byte of the bf16 entry V[m][c].  Codes 8..15 are stored
-// in reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.  Rows are laid
-// out in blocks of eight: the eight low-byte chunks, then the eight high-byte chunks, so the chunk
-// of row m sits at index m + (m & ~7) (+ 8 for the high bytes) and eight lanes reading random rows
-// spread over all eight 16-byte bank groups of a 128-byte line.
+// V table.  Row R holds the 16 bf16 entries of one scale class as two 16-byte chunks: the low bytes
+// {L(0..3), L(4..7), L(15..12), L(11..8)} at chunk R and the high bytes in the same order at chunk
+// kVtabHi + R, L / H being the low / high byte of the entry for code c.  Codes 8..15 are stored in
+// reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.
 // Rows 0..1023 hold V[m][c] = bf16(fp32(T[c] * (1 + m/1024))); rows 1024..2047 hold 2 * V[m][c] (the
-// same values one binade up, exact); row 2048 is all zeros.  The GEMV reads rows 0..1023 (the first
-// 2048 chunks); the small-M streaming kernel reads all of them.
+// same values one binade up, exact); row 2048 is all zeros.  The GEMV and the GEMM-form streaming
+// kernel read rows 0..1023; the small-M streaming kernel reads all of them.
 constexpr int kVtabRows = 2049;
-constexpr int kVtabChunks = 2 * 2048 + 16;  // chunk index of row 2048's high bytes is 4104
+constexpr int kVtabHi = 2056;                  // first high-byte chunk
+constexpr int kVtabChunks = kVtabHi + 2056;    // 4112 chunks (65,792 bytes)
 __device__ uint4 g_vtab[kVtabChunks];
 
 __global__ void build_vtab_kernel() {
@@ -67,9 +66,13 @@ __global__ void build_vtab_kernel() {
             hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
         }
     }
-    g_vtab[row + (row & ~7)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    g_vtab[row + (row & ~7) + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    g_vtab[row] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    g_vtab[kVtabHi + row] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
+
+// Shared-memory copy of rows 0..1023 for the GEMV and the GEMM-form kernel: 1024 low-byte chunks,
+// then 1024 high-byte chunks (32 KB).  Chunk i of the copy.
+__device__ __forceinline__ const uint4* vtab_src32k(int i) { return &g_vtab[i < 1024 ? i : kVtabHi + (i - 1024)]; }
 
 // Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order.
 // 18 ALU-pipe instructions (PRMT / LOP3) and 4 FMA-pipe ones (selector preparation).
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
         // The V table is for the consumers alone: they copy it while the producer already streams
         // the first row blocks, and meet on a named barrier before the first lookup.
-        for (int i = threadIdx.x; i < kVtabBytes / 16; i += 32 * C) cp_async16(smem + 16 * i, &g_vtab[i]);
+        for (int i = threadIdx.x; i < kVtabBytes / 16; i += 32 * C) cp_async16(smem + 16 * i, vtab_src32k(i));
         cp_async_commit();
         pdl_wait();
         uint32_t xr[MT][WPL / 2];
@@ -355,8 +358,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
                 const uint32_t m = (sb >> 13) & 0x3FFu;
                 pow2[jj] = __uint_as_float(sb & 0xFF800000u);  // +-2^E, or 0 for a zero scale
-                tl[jj] = vtab[m + (m & ~7u)];
-                th[jj] = vtab[m + (m & ~7u) + 8];
+                tl[jj] = vtab[m];
+                th[jj] = vtab[1024 + m];
             }
 #pragma unroll
             for (int jj = 0; jj < RMAX; jj++) {
@@ -581,6 +584,10 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     int kThreads;
     void (*kernel)(const CUtensorMap, const CUtensorMap, const st::CodeMaps, const st::Params);
     if constexpr (T <= 32) {
+        // the narrow kernel's B tile holds T tokens x s_rem slices (its shared memory is sized for it)
+        if (P.s_rem < 1 || P.s_rem > st::NCfg<T>::kSMax || (P.s_rem & (P.s_rem - 1)) != 0 ||
+            T * P.s_rem > st::NCfg<T>::kJMax)
+            return cudaErrorInvalidValue;
         kBytes = st::NCfg<T>::kBytes;
         kThreads = st::NCfg<T>::kThreads;
         kernel = st::narrow_kernel<T>;
@@ -689,33 +696,36 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
     P.p16 = 0x10000u;
     // K-slices of a partial tile: as many as fit 128 MMA rows, the B tile's pseudo-token columns and G.
     P.r_rem = static_cast<int>(rpc % 128);
+    // (a power of two, so that a row's slices are consecutive lanes of one warp)
     auto slices = [&](int smax) {
         int64_t s = P.r_rem ? 128 / P.r_rem : 1;
         if (s > smax) s = smax;
         if (s > G) s = G;
-        return static_cast<int>(s < 1 ? 1 : s);
+        int p2 = 1;
+        while (2 * p2 <= s) p2 *= 2;
+        return p2;
     };
     if (M == 1) {
-        P.s_rem = slices(st::Cfg<1>::kSMax);
+        P.s_rem = slices(st::NCfg<1>::kSMax);
         return launch_stream_t<1>(x, P, M, K, stream);
     }
     if (M == 2) {
-        P.s_rem = slices(st::Cfg<2>::kSMax);
+        P.s_rem = slices(st::NCfg<2>::kSMax);
         return launch_stream_t<2>(x, P, M, K, stream);
     }
     if (M <= 4) {
-        P.s_rem = slices(st::Cfg<4>::kSMax);
+        P.s_rem = slices(st::NCfg<4>::kSMax);
         return launch_stream_t<4>(x, P, M, K, stream);
     }
     if (M <= 8) {
-        P.s_rem = slices(st::Cfg<8>::kSMax);
+        P.s_rem = slices(st::NCfg<8>::kSMax);
         return launch_stream_t<8>(x, P, M, K, stream);
     }
     if (M <= 16) {
-        P.s_rem = slices(st::Cfg<16>::kSMax);
+        P.s_rem = slices(st::NCfg<16>::kSMax);
         return launch_stream_t<16>(x, P, M, K, stream);
     }
-    P.s_rem = slices(st::Cfg<32>::kSMax);
+    P.s_rem = slices(st::NCfg<32>::kSMax);
     return launch_stream_t<32>(x, P, M, K, stream);
 }
 

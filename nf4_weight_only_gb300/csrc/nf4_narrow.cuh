@@ -18,9 +18,11 @@
 // one CTA per SM with a balanced row range each.
 //
 // Pipeline stage = 128 k per MMA row (two 64-k sub-stages, 8 MMAs of K = 16).  Stage q uses A slot
-// q mod NA in tensor memory and x slot q mod NA in shared memory (both sub-tiles of the stage), so
-// one tcgen05.commit per stage frees both.  The MMA warp waits twice per stage (x landed, A written)
-// and commits once; it runs converged and one elected lane issues (see elect_one).
+// q mod 4 in tensor memory and x slot q mod 4 in shared memory (both sub-tiles of the stage), so one
+// tcgen05.commit per stage frees both.  Two MMA warps take alternate stages, each into its own pair
+// of accumulators, so that issuing costs the same on two warp schedulers; an issuer waits twice per
+// stage (x landed, A written) and commits once, converged, one elected lane issuing (elect_one).
+// The epilogue adds the four accumulators in a fixed order.
 //
 // Exponent folding.  A nonzero scale is 2^E * (1 + m/1024) with E = 2q + p, p in {0, 1}.  The table
 // row 1024 p + m holds 2^p * V[m][c] = bf16(T[c] * 2^p * (1 + m/1024)) exactly (rounding commutes
@@ -29,11 +31,15 @@
 // negative scale (never produced by nf4_quantize, but allowed) flips the sign bits of the nonzero
 // entries on a warp-uniform branch.
 //
-// Warp roles: warp 0 streams codes (TMA) and scale windows, warp 1 owns tensor memory and issues the
-// MMAs, warps 2 .. 4*kSets+1 are kSets sets of four dequant warps (a set takes every kSets-th stage;
-// the four warps of a set cover the four 32-lane quarters of tensor memory) that also run the
-// epilogue of every kSets-th tile, and the last warp streams x.  Weights do not depend on the
-// previous kernel in the stream, so warp 0 never waits for it; only x and y do.
+// Warp roles, one helper per warp scheduler (warp w runs on scheduler w mod 4): warp 0 streams codes
+// (TMA), warps 1 and 3 issue the MMAs of even and odd stages (warp 1 also owns tensor memory), warp 2
+// streams x; warps 4 .. 4*kSets+3 are kSets sets of four dequant warps (a set takes every kSets-th
+// stage; the four warps of a set cover the four 32-lane quarters of tensor memory, one per
+// scheduler) that also run the epilogue of every kSets-th tile.  A set's stage is done when its
+// slowest warp is, so every scheduler carries the same load.  Each dequant thread reads its own
+// group scales from global memory two of its stages ahead (no staging, no barrier).  Weights do not
+// depend on the previous kernel in the stream, so warp 0 and the scale loads never wait for it;
+// only x and y do.
 // Every mbarrier wait is bounded (wall clock, per wait); a wait that runs out records an error code,
 // the roles drain the copies and MMAs in flight (bounded again) and tensor memory is always freed.
 #pragma once
@@ -41,30 +47,32 @@
 namespace nf4 {
 namespace st {
 
+// Ring depths are powers of two (slot and phase arithmetic are masks and shifts).  K-slices are a
+// power of two no larger than kSMax, so a row's slices sit in consecutive lanes of one warp and the
+// epilogue adds them with shuffles.
 template <int T>
 struct NCfg {
-    static constexpr int kJMax = T == 1 ? 16 : (T <= 4 ? 32 : 64);  // columns of B and of each D
+    static constexpr int kJMax = T <= 2 ? 16 : (T == 4 ? 32 : 64);  // columns of B and of each D
     static constexpr int kSMax = kJMax / T < 8 ? kJMax / T : 8;        // K-slices per tile
-    static constexpr int kAccN = 4;                                    // K-step k8 -> accumulator k8 % 4
+    static constexpr int kAccN = 4;                                    // two per MMA warp
     static constexpr int kDCols = kAccN * kJMax;
-    static constexpr int kAStages = ((512 - kDCols) / 64 < 8 ? (512 - kDCols) / 64 : 8) & ~1;
+    static constexpr int kAStages = 4;                                 // A slots (tensor memory) = x slots
+    static constexpr int kLoadStages = 4;                              // codes load stages
     static constexpr int kSets = 3;
-    static constexpr int kXWarp = 2 + 4 * kSets;
-    static constexpr int kThreads = 32 * (kXWarp + 1);
-    static constexpr int kLoadStages = T >= 16 ? 3 : 4;
-    static constexpr int kScaleStages = 3;
+    static constexpr int kThreads = 32 * (4 + 4 * kSets);             // 4 helper warps, one per scheduler
+    static constexpr int kU = 4;                                       // 64-k sub-stages per codes load stage
     static constexpr uint32_t kXSub = kJMax * 128;  // one 64-k x sub-tile (multiple of 1024 bytes)
     static constexpr uint32_t kXSlot = 2 * kXSub;
     static constexpr uint32_t kVtabBytes = kVtabChunks * 16;
     static constexpr uint32_t kOffCodes = kAStages * kXSlot;
     static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
-    static constexpr uint32_t kOffScales = kOffVtab + kVtabBytes;
-    static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
-    static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
+    static constexpr uint32_t kOffBars = kOffVtab + kVtabBytes;
     static constexpr uint32_t kBytes = kOffBars + 1024;
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(kDCols + 64 * kAStages <= 512, "tensor memory budget");
-    static_assert(8 * (2 * kLoadStages + 3 * kAStages + 2 * kScaleStages + 2 * kSets + 2) + 4 <= 1024, "barrier area");
+    static_assert(kAStages == 4 && kLoadStages == 4, "slot arithmetic assumes rings of four");
+    static_assert(kSMax == 1 || kSMax == 2 || kSMax == 4 || kSMax == 8, "slices are a power of two");
+    static_assert(8 * (2 * kLoadStages + 3 * kAStages + kSets + 3) + 4 <= 1024, "barrier area");
 };
 
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane, without waiting for the store.
@@ -79,12 +87,17 @@ __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t 
         : "memory");
 }
 
+// Group scale `g` of a row (bits), or 0 when g is past the row or the lane has no row.
+__device__ __forceinline__ uint32_t load_scale(const uint16_t* row_scales, int g, int G, bool lane_ok) {
+    return (lane_ok && g < G) ? static_cast<uint32_t>(ld_nc_u16(row_scales + g)) : 0u;
+}
+
 template <int T>
 __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
     narrow_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
                   const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
     using C = NCfg<T>;
-    constexpr int NA = C::kAStages, NL = C::kLoadStages, NSS = C::kScaleStages;
+    constexpr int NA = C::kAStages, NL = C::kLoadStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -97,13 +110,10 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
     const uint32_t b_xfull = b_lempty + 8 * NL;     // [NA] x slot landed (tx)
     const uint32_t b_afull = b_xfull + 8 * NA;      // [NA] A slot written (4 warps)
     const uint32_t b_empty = b_afull + 8 * NA;      // [NA] A and x slot read by the MMAs (commit)
-    const uint32_t b_sfull = b_empty + 8 * NA;      // [NSS] scale tile landed (32 producer lanes)
-    const uint32_t b_sempty = b_sfull + 8 * NSS;    // [NSS] scale tile read (weighted releases)
-    const uint32_t b_dfull = b_sempty + 8 * NSS;    // [kSets] accumulators complete (commit), per epilogue set
-    const uint32_t b_ep = b_dfull + 8 * C::kSets;   // [kSets] per-set epilogue rendezvous
-    const uint32_t b_dfree = b_ep + 8 * C::kSets;   // accumulators read (4 warps)
-    const uint32_t b_mdone = b_dfree + 8;           // every MMA issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * NL + 3 * NA + 2 * NSS + 2 * C::kSets + 2));
+    const uint32_t b_dfull = b_empty + 8 * NA;      // [kSets] accumulators complete (both MMA warps), per epilogue set
+    const uint32_t b_dfree = b_dfull + 8 * C::kSets;  // accumulators read (4 warps)
+    const uint32_t b_mdone = b_dfree + 8;           // [2] every MMA an MMA warp issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * NL + 3 * NA + C::kSets + 3));
 
     // this CTA's problem and rows
     int p = 0;
@@ -125,16 +135,10 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             mbar_init(b_afull + 8 * i, 4);
             mbar_init(b_empty + 8 * i, 1);
         }
-        for (int i = 0; i < NSS; i++) {
-            mbar_init(b_sfull + 8 * i, 32);
-            mbar_init(b_sempty + 8 * i, 48);
-        }
-        for (int i = 0; i < C::kSets; i++) {
-            mbar_init(b_dfull + 8 * i, 1);
-            mbar_init(b_ep + 8 * i, 4);
-        }
+        for (int i = 0; i < C::kSets; i++) mbar_init(b_dfull + 8 * i, 2);
         mbar_init(b_dfree, 4);
         mbar_init(b_mdone, 1);
+        mbar_init(b_mdone + 8, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -153,10 +157,10 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
     const uint64_t wait_ns = g_wait_ns;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- codes and scales
-        // Lane 0 issues the TMA boxes (elected, converged warp); the warp copies scale windows.
-        const uint8_t* sbytes = reinterpret_cast<const uint8_t*>(P.scales[p]);
-        const int64_t s_total = static_cast<int64_t>(P.n[p]) * G * 2;
+        // ---------------------------------------------------------------- codes
+        // One elected lane of the converged warp issues the TMA boxes.  A load stage is four 64-k
+        // sub-stages of every row of the tile: one box of 128-byte rows (S = 1), two (S = 2) or four
+        // (S >= 4, one per sub-stage), each box at its own quarter, half or whole of the slot.
         const CUtensorMap* cm_full = &cmaps.full[p];
         const CUtensorMap* cm_rem = &cmaps.rem[p];
         if (lane == 0) {
@@ -165,63 +169,32 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         }
         __syncwarp();
         bool ok = true;
-        int lq = 0, lslot = 0, lround = 0, sslot = 0, sround = 0;
+        int lq = 0;
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
-            const int U = load_span(t.s);
             const CUtensorMap* cmap = t.s > 1 ? cm_rem : cm_full;
-            const uint32_t cbytes = t.s > 1 ? 32u * U * t.s * P.r_rem : kLoadBytes;  // all boxes of a stage
             const int BS = box_span(t.s);
-            const uint32_t per_row = (t.s + 2) * 16;
-            for (int kb = 0, g = 0; kb < t.nt; kb++, g += t.s) {
-                if ((kb & (U - 1)) == 0) {  // codes load stage: all rows x U*S groups
-                    if (lround > 0 && !warp_wait(b_lempty + 8 * lslot, (lround - 1) & 1, wait_ns)) {
-                        if (lane == 0) record_error(21);
-                        ok = false;
-                        break;
-                    }
-                    expect_tx_elect(b_lfull + 8 * lslot, cbytes);
-                    for (int b = 0; b < U / BS; b++)
-                        tma_load_2d_elect(sbase + C::kOffCodes + lslot * kLoadBytes + b * kBoxStride, cmap,
-                                          (g + b * BS * t.s) * 32, t.row0, b_lfull + 8 * lslot);
-                    lq++;
-                    if (++lslot == NL) {
-                        lslot = 0;
-                        lround++;
-                    }
+            const int nbox = C::kU / BS;
+            const uint32_t bstride = kLoadBytes / nbox;
+            const uint32_t cbytes = t.s > 1 ? 32u * C::kU * t.s * P.r_rem : kLoadBytes;  // all boxes of a stage
+            for (int kb = 0; kb < t.nt; kb += C::kU, lq++) {  // codes load stage: all rows x 4S groups
+                const int lslot = lq & (NL - 1), lround = lq >> 2;
+                if (lround > 0 && !warp_wait(b_lempty + 8 * lslot, (lround - 1) & 1, wait_ns)) {
+                    if (lane == 0) record_error(21);
+                    ok = false;
+                    break;
                 }
-                if ((kb & 7) == 0) {  // scale tile: groups g .. g + 8S - 1 of every row
-                    if (sround > 0 && !warp_wait(b_sempty + 8 * sslot, (sround - 1) & 1, wait_ns)) {
-                        if (lane == 0) record_error(22);
-                        ok = false;
-                        break;
-                    }
-                    const int g1 = g + 8 * t.s < G ? g + 8 * t.s : G;
-                    uint8_t* dst = smem + C::kOffScales + sslot * kScaleSlot;
-                    for (int r = lane; r < t.rows; r += 32) {
-                        const int64_t rb = static_cast<int64_t>(t.row0 + r) * G * 2;
-                        const int64_t a = (rb + 2 * g) & ~static_cast<int64_t>(15);
-                        for (int64_t c = a; c < rb + 2 * g1; c += 16) {
-                            const int64_t left = s_total - c;
-                            cp_async16(dst + r * per_row + (c - a), sbytes + c, static_cast<uint32_t>(left < 16 ? left : 16));
-                        }
-                    }
-                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b_sfull + 8 * sslot)
-                                 : "memory");
-                    if (++sslot == NSS) {
-                        sslot = 0;
-                        sround++;
-                    }
-                }
-                __syncwarp();
+                expect_tx_elect(b_lfull + 8 * lslot, cbytes);
+                for (int b = 0; b < nbox; b++)
+                    tma_load_2d_elect(sbase + C::kOffCodes + lslot * kLoadBytes + b * bstride, cmap,
+                                      (kb + b * BS) * t.s * 32, t.row0, b_lfull + 8 * lslot);
             }
         }
-        cp_async_wait<0>();
         // drain: the codes of the last ring round have landed before the CTA may exit
-        for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq % NL), (qq / NL) & 1, kDrainNs);
-    } else if (warp == C::kXWarp) {
+        for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq & (NL - 1)), (qq >> 2) & 1, kDrainNs);
+    } else if (warp == 2) {
         // ---------------------------------------------------------------- x
-        // Stage q's two 64-k sub-tiles land in x slot q mod NA, counted on that slot's own barrier.
+        // Stage q's two 64-k sub-tiles land in x slot q mod 4, counted on that slot's own barrier.
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
@@ -235,7 +208,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
             const uint32_t subbytes = 128u * t.s * T;
             for (int kb2 = 0; kb2 < t.nt / 2; kb2++, q++) {
-                const int slot = q % NA, round = q / NA;
+                const int slot = q & (NA - 1), round = q >> 2;
                 if (round > 0 && !warp_wait(b_empty + 8 * slot, (round - 1) & 1, wait_ns)) {
                     if (lane == 0) record_error(23);
                     ok = false;
@@ -248,14 +221,20 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             }
         }
         // drain: the x slots of the last ring round have landed before the CTA may exit
-        for (int qq = q - NA > 0 ? q - NA : 0; qq < q; qq++) mbar_wait(b_xfull + 8 * (qq % NA), (qq / NA) & 1, kDrainNs);
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // The whole warp runs the loop (every operand warp-uniform); one elected lane issues.
+        for (int qq = q - NA > 0 ? q - NA : 0; qq < q; qq++) mbar_wait(b_xfull + 8 * (qq & (NA - 1)), (qq >> 2) & 1, kDrainNs);
+    } else if (warp == 1 || warp == 3) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Warp 1 issues the stages with even CTA-wide index into accumulators 0 and 1, warp 3 the odd
+        // ones into accumulators 2 and 3 (K-steps alternate between the pair).  The whole warp runs
+        // the loop (every operand warp-uniform); one elected lane issues.  Both commit every tile's
+        // end to the epilogue set's barrier, whether or not they had a stage in the tile.
+        const int e = warp == 1 ? 0 : 1;
+        const uint32_t acc0 = tmem_base + 2 * e * C::kJMax;
         bool ok = true;
-        int q = 0;
+        int q0 = 0;
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
+            const int nst = t.nt / 2;
             const int nmma = (T * t.s + 15) & ~15;
             const uint32_t idesc = idesc_n(nmma < 16 ? 16 : nmma);
             if (j > 0 && !warp_wait(b_dfree, (j - 1) & 1, wait_ns)) {
@@ -264,9 +243,11 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            for (int kb2 = 0; kb2 < t.nt / 2; kb2++, q++) {
-                const int slot = q % NA;
-                const uint32_t par = (q / NA) & 1;
+            bool first = true;
+            for (int kb2 = (q0 & 1) == e ? 0 : 1; kb2 < nst; kb2 += 2) {
+                const int q = q0 + kb2;
+                const int slot = q & (NA - 1);
+                const uint32_t par = (q >> 2) & 1;
                 if (!warp_wait(b_xfull + 8 * slot, par, wait_ns) || !warp_wait(b_afull + 8 * slot, par, wait_ns)) {
                     if (lane == 0) record_error(25);
                     ok = false;
@@ -278,51 +259,49 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
 #pragma unroll
                 for (int k8 = 0; k8 < 8; k8++) {  // K = 16 per MMA: 8 columns of A, 32 bytes of a B row
                     const uint64_t b = bdesc + (k8 >= 4 ? (C::kXSub >> 4) : 0) + 2 * (k8 & 3);
-                    mma_tmem_a_elect(tmem_base + (k8 % C::kAccN) * C::kJMax, a_tmem + 8 * k8, b, idesc,
-                                     kb2 > 0 || k8 >= C::kAccN);
+                    mma_tmem_a_elect(acc0 + (k8 & 1) * C::kJMax, a_tmem + 8 * k8, b, idesc, !first || k8 >= 2);
                 }
                 mma_commit_elect(b_empty + 8 * slot);
+                first = false;
             }
-            if (ok) mma_commit_elect(b_dfull + 8 * (j % C::kSets));
+            if (!ok) break;
+            mma_commit_elect(b_dfull + 8 * (j % C::kSets));
+            q0 += nst;
         }
-        mma_commit_elect(b_mdone);  // the CTA exits only after every MMA it issued has completed
-        mbar_wait(b_mdone, 0, kDrainNs);
+        mma_commit_elect(b_mdone + 8 * e);  // the CTA exits only after every MMA it issued has completed
+        mbar_wait(b_mdone + 8 * e, 0, kDrainNs);
     } else {
         // ---------------------------------------------------------------- dequant + epilogue
-        const int set = (warp - 2) >> 2;
+        const int set = (warp - 4) >> 2;
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
         const int i = quarter * 32 + lane;        // MMA row
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint4* vtab = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
+        const uint4* vt_lo = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
+        const uint4* vt_hi = vt_lo + kVtabHi;
         bool ok = true;
-        int ep_uses = 0;
-        // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
-        // ring slots and phases follow from them, so a set visits only its own stages.
-        int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
-        // A warp waits only for the codes load stage and the scale tile of its own stages, and its
-        // set releases them after use; the release counts are weighted so that a slot completes when
-        // every stage that reads it is done (a load stage: 8 = two stages of four warps, or one at
-        // weight 2; a scale tile: 48 = n stages of four warps at weight 12 / n).  A parity wait is
-        // sound when the slot's previous fill has completed and its next cannot have: the next
-        // needs this warp's own release, and the previous is complete once the fills are at most
-        // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
-        // A set's stages are kSets apart; a load stage holds two stages (S = 1) or one, a scale tile
-        // four.  The A slot of a stage is reused NA stages later; a set's previous stage (kSets
-        // earlier) waited for the slot of kSets + NA stages back, so with NA >= kSets the wait for
-        // the slot's previous use (NA back) is on a phase whose predecessor has completed.
-        static_assert(C::kSets <= NL && C::kSets <= NA && NSS >= 2, "ring too shallow for the release rule");
+        // CTA-wide counts of the stages and codes load stages of the tiles before tile j: ring slots
+        // and phases follow from them, so a set visits only its own stages.
+        int q0 = 0, l0 = 0;
+        // A warp waits only for the codes load stage of its own stages, and its set releases it
+        // after use; the release counts are weighted so that a slot completes when every stage that
+        // reads it is done (8 = two stages of four warps, or one at weight 2).  A parity wait is
+        // sound when the slot's previous fill has completed and its next cannot have: the next needs
+        // this warp's own release, and the previous is complete once the fills are at most NL apart
+        // between consecutive stages of a set, because the warp saw the earlier one.  A set's stages
+        // are kSets apart and a load stage holds two.  The A slot of a stage is reused NA stages
+        // later; a set's previous stage (kSets earlier) waited for the slot of kSets + NA stages
+        // back, so with NA >= kSets the wait for the slot's previous use (NA back) is on a phase whose
+        // predecessor has completed.
+        static_assert(C::kSets <= NL && C::kSets <= NA, "ring too shallow for the release rule");
         for (int j = 0; j < ntiles && ok; j++) {
-            q0 += nst_prev;
-            l0 += nload_prev;
-            s0 += nscale_prev;
             const Tile t = tile_of(P, rbeg, rows_cta, j);
-            const int U = load_span(t.s), BS = box_span(t.s);
-            const int lbs = BS == 4 ? 2 : (BS == 2 ? 1 : 0);  // log2 BS
-            const int nst = t.nt / 2, nload = (t.nt + U - 1) / U, nscale = (t.nt + 7) / 8;
-            nst_prev = nst;
-            nload_prev = nload;
-            nscale_prev = nscale;
-            const int r = i / t.s, sl = i - (i / t.s) * t.s;
+            constexpr int lu = 2;                                 // log2 of the sub-stages per load stage
+            const int BS = box_span(t.s);
+            const int lbs = BS == 4 ? 2 : (BS == 2 ? 1 : 0);      // log2 BS
+            const uint32_t bstride = kLoadBytes >> (lu - lbs);    // a load stage holds 4 / BS boxes
+            const int ls = t.s == 8 ? 3 : (t.s == 4 ? 2 : (t.s == 2 ? 1 : 0));  // log2 S
+            const int nst = t.nt / 2, nload = (t.nt + C::kU - 1) / C::kU;
+            const int r = i >> ls, sl = i & (t.s - 1);
             const bool lane_ok = r < t.rows;
             const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
             // codes of row r in a box: rowb bytes, 16-byte chunks permuted by the 128-byte swizzle
@@ -330,21 +309,26 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const uint32_t rowb = 32u * BS * t.s;
             const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
             const uint8_t* crow0 = smem + C::kOffCodes + r * rowb;
-            // this lane's scale inside a scale tile: row r's window starts at the 16-byte boundary
-            // below its first scale; sub-stage kb adds 2 * (kb mod 8) * S bytes
-            const uint8_t* srow0 = smem + C::kOffScales +
-                                   (r * (t.s + 2) * 16 + static_cast<uint32_t>((static_cast<int64_t>(t.row0 + r) * G * 2) & 15) + 2 * sl);
-            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets)
-            for (int kb2 = (set - q0 % C::kSets + C::kSets) % C::kSets; kb2 < nst && ok; kb2 += C::kSets) {
+            const uint16_t* row_scales = P.scales[p] + static_cast<int64_t>(t.row0 + (lane_ok ? r : 0)) * G;
+            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets); scales two stages ahead
+            const int kfirst = (set - q0 % C::kSets + C::kSets) % C::kSets;
+            uint32_t sc_n[2], sc_n1[2], sc_n2[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                sc_n[h] = load_scale(row_scales, ((2 * kfirst + h) << ls) + sl, G, lane_ok);
+                sc_n1[h] = load_scale(row_scales, ((2 * (kfirst + C::kSets) + h) << ls) + sl, G, lane_ok);
+            }
+            for (int kb2 = kfirst; kb2 < nst && ok; kb2 += C::kSets) {
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+                    sc_n2[h] = load_scale(row_scales, ((2 * (kb2 + 2 * C::kSets) + h) << ls) + sl, G, lane_ok);
                 const int gq = q0 + kb2;
-                const int aslot = gq % NA, around = gq / NA;
+                const int aslot = gq & (NA - 1), around = gq >> 2;
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
-                const int li = kbs / U;                   // its codes load stage, tile-relative
-                const int si = kbs >> 3;                  // its scale tile, tile-relative
-                const int L = l0 + li, S = s0 + si;       // CTA-wide
-                const int lslot = L % NL, sslot = S % NSS;
-                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, wait_ns) &&
-                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, wait_ns);
+                const int li = kbs >> lu;                 // its codes load stage, tile-relative
+                const int L = l0 + li;                    // CTA-wide
+                const int lslot = L & (NL - 1);
+                bool good = warp_wait(b_lfull + 8 * lslot, (L >> 2) & 1, wait_ns);
                 if (good && around > 0) good = warp_wait(b_empty + 8 * aslot, (around - 1) & 1, wait_ns);
                 if (!good) {
                     if (lane == 0) record_error(26);
@@ -353,35 +337,34 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 }
                 tc_fence_after();
                 if (warp_ok) {
+                    const uint8_t* crow = crow0 + lslot * kLoadBytes;
 #pragma unroll 1
                     for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
                         const int kb = kbs + h;
-                        const int u = kb & (U - 1);  // sub-stage in the load stage: box u / BS
+                        const int u = kb & (C::kU - 1);  // sub-stage in the load stage: box u / BS
                         uint32_t out[32];
-                        const int g = kb * t.s + sl;
+                        const int g = (kb << ls) + sl;
                         if (lane_ok && g < G) {
-                            const uint8_t* crow = crow0 + lslot * kLoadBytes + (u >> lbs) * kBoxStride;
-                            const uint32_t ch = static_cast<uint32_t>(((u & (BS - 1)) * t.s + sl) * 2);
-                            const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
-                            const uint16_t sc = *reinterpret_cast<const uint16_t*>(srow0 + sslot * kScaleSlot + 2 * (kb & 7) * t.s);
-                            // scale = sign * 2^(2q + p) * (1 + m/1024): row 1024 p + m of the table, q
-                            // added to the high byte of every nonzero entry (code 7's byte stays 0)
-                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
-                            const uint32_t mag = sb & 0x7FFFFFFFu;
-                            const uint32_t nz = mag != 0u ? 1u : 0u;
-                            const uint32_t e = mag >> 23;
-                            const uint32_t pbit = (e & 1u) ^ 1u;                       // (e - 127) mod 2
-                            const int q = (static_cast<int>(e) - 127 - static_cast<int>(pbit)) >> 1;
-                            const uint32_t row = nz ? ((mag >> 13) & 0x3FFu) + (pbit << 10) : 2048u;
-                            const uint32_t qq = static_cast<uint32_t>(q) * nz;
-                            uint4 tl = vtab[row + (row & ~7u)];
-                            uint4 th = vtab[row + (row & ~7u) + 8];
+                            const uint8_t* cb = crow + (u >> lbs) * bstride;
+                            const uint32_t ch = static_cast<uint32_t>((((u & (BS - 1)) << ls) + sl) * 2);
+                            const uint4 c0 = lds128(cb + 16 * (ch ^ swz)), c1 = lds128(cb + 16 * ((ch + 1) ^ swz));
+                            // scale = sign * 2^E * (1 + m/1024), E = e - 127 = 2q + p: table row
+                            // 1024 p + m, and q added to the high byte of every nonzero entry (code 7's
+                            // byte stays 0); a zero scale reads the zero row
+                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1]))));
+                            const uint32_t e = (sb >> 23) & 0xFFu;
+                            const uint32_t hq = (e + 1u) >> 1;                   // q + 64
+                            const uint32_t pbit = e + 1u - 2u * hq;
+                            const uint32_t row = e != 0u ? ((sb >> 13) & 0x3FFu) + (pbit << 10) : 2048u;
+                            const uint32_t qq = e != 0u ? hq - 64u : 0u;
+                            const uint4 tl = vt_lo[row];
+                            uint4 th = vt_hi[row];
                             th.x += qq * 0x01010101u;
                             th.y += qq * 0x00010101u;
                             th.z += qq * 0x01010101u;
                             th.w += qq * 0x01010101u;
                             if (__any_sync(__activemask(), (sb >> 31) != 0u)) {  // a negative scale (rare)
-                                const uint32_t sg = ((sb >> 31) != 0u && nz) ? 0x80808080u : 0u;
+                                const uint32_t sg = ((sb >> 31) != 0u && e != 0u) ? 0x80808080u : 0u;
                                 th.x ^= sg;
                                 th.y ^= sg & 0x00FFFFFFu;
                                 th.z ^= sg;
@@ -409,12 +392,20 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(b_afull + 8 * aslot);
-                    const int touching = U == 4 ? (nst - 2 * li < 2 ? nst - 2 * li : 2) : 1;
-                    mbar_arrive_count(b_lempty + 8 * lslot, 2 / touching);
-                    const int stouch = nst - 4 * si < 4 ? nst - 4 * si : 4;
-                    mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
+                    // a load stage is read by two pipeline stages (weight 1 each), unless it holds
+                    // the tile's last stage alone (weight 2)
+                    mbar_arrive_count(b_lempty + 8 * lslot, nst - 2 * li >= 2 ? 1 : 2);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    sc_n[h] = sc_n1[h];
+                    sc_n1[h] = sc_n2[h];
                 }
             }
+            // which MMA warps had a stage in this tile (the other's accumulators were not written)
+            const bool has0 = nst >= 2 || (q0 & 1) == 0, has1 = nst >= 2 || (q0 & 1) == 1;
+            q0 += nst;
+            l0 += nload;
             if (!ok || j % C::kSets != set) continue;
             // ------------------------------------------------------------ epilogue of tile j
             if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, wait_ns)) {
@@ -426,45 +417,45 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             pdl_wait();  // y may still be read by the previous grid (returns at once by now)
             const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
             uint16_t* y = P.y[p];
-            float* red = reinterpret_cast<float*>(smem + C::kOffRed);
             const int J = T * t.s;
             for (int c = 0; c < J; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_base + lane_addr + c, v);
+                // accumulators 0 + 1 (even stages), then 2 + 3 (odd stages), then their sum
+                float v[16];
 #pragma unroll
-                for (int a = 1; a < C::kAccN; a++) {  // add the accumulators in order
-                    uint32_t w[16];
-                    tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
+                for (int cc = 0; cc < 16; cc++) v[cc] = 0.0f;
 #pragma unroll
-                    for (int cc = 0; cc < 16; cc++) v[cc] = __float_as_uint(__uint_as_float(v[cc]) + __uint_as_float(w[cc]));
+                for (int pr = 0; pr < 2; pr++) {
+                    if (!(pr == 0 ? has0 : has1)) continue;  // warp-uniform
+                    uint32_t a[16], b[16];
+                    tmem_ld16(tmem_base + lane_addr + (2 * pr) * C::kJMax + c, a);
+                    tmem_ld16(tmem_base + lane_addr + (2 * pr + 1) * C::kJMax + c, b);
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++) v[cc] += __uint_as_float(a[cc]) + __uint_as_float(b[cc]);
                 }
+                if (t.s == 1) {
 #pragma unroll
-                for (int cc = 0; cc < 16; cc++) {
-                    const int col = c + cc;
-                    if (t.s == 1) {
+                    for (int cc = 0; cc < 16; cc++) {
+                        const int col = c + cc;
                         if (lane_ok && col < M)
-                            y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
-                    } else {
-                        const int rel = col - sl;
-                        const int tt = rel / t.s;
-                        if (rel >= 0 && rel == tt * t.s && tt < M) red[tt * 128 + i] = __uint_as_float(v[cc]);
+                            y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(v[cc]);
                     }
-                }
-            }
-            if (C::kSMax > 1 && t.s > 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_ep + 8 * set);
-                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
-                    if (lane == 0) record_error(27);
-                    ok = false;
-                    break;
-                }
-                ep_uses++;
-                for (int o = i; o < t.rows * M; o += 128) {
-                    const int tt = o / t.rows, rr = o - tt * t.rows;
-                    float acc = 0.0f;
-                    for (int s2 = 0; s2 < t.s; s2++) acc += red[tt * 128 + rr * t.s + s2];
-                    y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = bf16_bits(acc);
+                } else {
+                    // column col = token * S + slice: this lane keeps its own slice's value of each
+                    // token, and after a token's last column the S lanes of the row add theirs with
+                    // shuffles (a fixed order: the result does not depend on timing)
+                    float val = 0.0f;
+#pragma unroll
+                    for (int cc = 0; cc < 16; cc++) {
+                        const int col = c + cc;
+                        if ((col & (t.s - 1)) == sl) val = v[cc];
+                        if ((col & (t.s - 1)) == t.s - 1) {  // warp-uniform
+                            float sum = val;
+                            for (int off = 1; off < t.s; off <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+                            const int tt = col >> ls;
+                            if (sl == 0 && lane_ok && tt < M)
+                                y[static_cast<int64_t>(m0 + tt) * np + t.row0 + r] = bf16_bits(sum);
+                        }
+                    }
                 }
             }
             tc_fence_before();

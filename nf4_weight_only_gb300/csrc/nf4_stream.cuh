@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < 2048; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
+    for (int i = threadIdx.x; i < 2048; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, vtab_src32k(i));
     cp_async_commit();
     cp_async_wait<0>();
     tc_fence_before();
@@ -574,8 +574,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                         const uint32_t pm = (e & 1) ? 0x80808080u : 0u;
                         const uint32_t add = static_cast<uint32_t>(e >> 1) * 0x01010101u;
                         const uint32_t sgn = (sb >> 31) ? 0x80808080u : 0u;
-                        uint4 tl = vtab[m + (m & ~7u)];
-                        uint4 th = vtab[m + (m & ~7u) + 8];
+                        uint4 tl = vtab[m];
+                        uint4 th = vtab[1024 + m];
                         th.x = (th.x + add + ((tl.x & pm) >> 7)) ^ sgn;
                         th.y = ((th.y + add + ((tl.y & pm) >> 7)) & 0x00FFFFFFu) ^ sgn;  // code 7 stays 0
                         th.z = (th.z + add + ((tl.z & pm) >> 7)) ^ sgn;
