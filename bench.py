@@ -1,12 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the NF4 weight-only linear layer on one GB300 (or N independent replicas).
 
-Headline: NF4 GEMV (M = 1) HBM GB/s on the packed bytes over one decode pass of the 3B-shaped
-workload (hidden 2048, 36 layers, 1.474 GB of codes + scales resident in HBM).  A step is one pass
-over every linear of every layer in dependency order -- per layer q|k|v (one grouped launch, shared
-input), o, gate|up (grouped), down: 144 launches chained with programmatic dependent launch and
-replayed from one CUDA graph.  The 20B-shaped prefill (M = 32 and M = 512) is timed after the
-headline loop and reported under "prefill".
+Headline: NF4 GEMV (M = 1) HBM GB/s on the packed bytes over one decode pass of the 32B-shaped
+weight sweep (hidden 5120, intermediate 27648, 64 layers, 16.58 GB of codes + scales resident in
+HBM).  A step is one pass over every linear of every layer in dependency order -- per layer q|k|v
+(one grouped launch, shared input), o, gate|up (grouped), down: 256 launches chained with
+programmatic dependent launch and replayed from one CUDA graph.
+
+Every other workload is reported beside it under "configs": the single 2048 x 2048 linear (weights
+rotated over more than four L2 sizes of copies, the hot-L2 figure labelled apart), the 3B-shaped
+decode pass, the 14B-shaped pass at M = 1, 4 and 8, and the 20B-shaped prefill at M = 32 and 512.
+The device error word of the bounded pipeline waits is read after every timed region, and the
+cpu_baseline leg checks sampled outputs of the headline's timed graph against the oracle.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch with torch.distributed.run; each rank runs a full replica (weak scaling).
@@ -21,6 +26,7 @@ import subprocess
 import sys
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -30,15 +36,20 @@ if ROOT not in sys.path:
 from nf4_weight_only_gb300 import workloads as W  # noqa: E402
 
 METRIC = "NF4 GEMV HBM GB/s (M=1) & % of peak; prefill TFLOP/s at M=32/512"
+HEADLINE = W.SWEEP_32B
 
 # One decoder layer's linears in dependency order; names in one tuple read the same input.
 LAYER_STEPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
 
-def decode_traffic_per_launch():
-    """DRAM bytes per decode launch from the committed ncu launch-list summary (None if absent)."""
+class BenchError(RuntimeError):
+    pass
+
+
+def traffic_per_launch(summary: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary (None if absent)."""
     import re
-    path = os.path.join(ROOT, "profiles", "gemv_decode_3b_launch_list.md")
+    path = os.path.join(ROOT, "profiles", summary)
     try:
         with open(path) as fh:
             m = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", fh.read(), re.M)
@@ -102,6 +113,14 @@ def clocks_summary(samples):
             "reasons": sorted({r for s in samples for r in s["reasons"]}), "samples": len(samples)}
 
 
+def check_device_error(nf4, where: str) -> None:
+    """The bounded pipeline waits record a code when one runs out (the launch's outputs are then
+    unspecified): a timed region that saw one is not a measurement."""
+    code = nf4.nf4_check_device_error()
+    if code:
+        raise BenchError(f"{where}: device error word {code} after the timed region")
+
+
 def timed_replays(graph, stream, steps, warmup, gpu_index):
     """`warmup` untimed replays, then exactly `steps` replays enqueued between CUDA events on
     `stream`; nvidia-smi is sampled while the device works through them.
@@ -124,10 +143,10 @@ def timed_replays(graph, stream, steps, warmup, gpu_index):
     return per, evs[0].elapsed_time(evs[-1]) / 1e3, samples
 
 
-def build_layers(nf4, synth, wl: W.Workload, dev):
+def build_layers(nf4, synth, wl: W.Workload, dev, layers: int = None):
     """Quantize every linear of every layer on the device (fp32 weights drawn there, then freed)."""
-    layers = []
-    for layer in range(wl.layers):
+    out = []
+    for layer in range(wl.layers if layers is None else layers):
         mats = {}
         for li, lin in enumerate(wl.linears):
             w = synth.device_weights(wl.seed * 100003 + layer * 16 + li, lin.n, lin.k, dev,
@@ -135,131 +154,181 @@ def build_layers(nf4, synth, wl: W.Workload, dev):
             codes, scales = nf4.quantize(w)
             del w
             mats[lin.name] = (lin, codes, scales)
-        layers.append(mats)
+        out.append(mats)
     torch.cuda.synchronize()
-    return layers
+    return out
 
 
-def run_ours(args, rank, world):
-    import nf4_weight_only_gb300 as nf4
-    from nf4_weight_only_gb300 import build, synth
+def run_pass(nf4, layers, xs, ys, stream):
+    """One pass in dependency order: per layer q|k|v (grouped), o, gate|up (grouped), down."""
+    for mats, yl in zip(layers, ys):
+        for names in LAYER_STEPS:
+            lin = mats[names[0]][0]
+            if len(names) == 1:
+                nf4.nf4_linear(xs[lin.k], mats[names[0]][1], mats[names[0]][2], yl[names[0]], stream)
+            else:
+                nf4.nf4_linear_grouped(xs[lin.k], [mats[n][1] for n in names], [mats[n][2] for n in names],
+                                       [yl[n] for n in names], stream)
 
-    build.build()
-    nf4.load()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    pk = peaks()
-    wl = W.DECODE_3B
-    layers = build_layers(nf4, synth, wl, dev)
-    xs = {k: synth.device_activations_bf16(77 + k, 1, k, dev) for k in {l.k for l in wl.linears}}
-    # every y is a view of one flat buffer (each n is a multiple of 8, so every view stays 16-byte
-    # aligned), which the end-to-end step copies back to the host in one transfer
-    y_flat = torch.empty(wl.layers * sum(lin.n for lin in wl.linears), dtype=torch.bfloat16, device=dev)
-    ys, off = [], 0
-    for m in layers:
-        yl = {}
-        for name, (lin, _, _) in m.items():
-            yl[name] = y_flat[off:off + lin.n].view(1, lin.n)
-            off += lin.n
-        ys.append(yl)
+
+class DecodePass:
+    """One decode pass of a layered workload at M tokens, captured in one CUDA graph.  Every y is a
+    view of one flat buffer (each n is a multiple of 8, so every view stays 16-byte aligned), which
+    the end-to-end step copies back in one transfer."""
+
+    def __init__(self, nf4, synth, wl: W.Workload, m: int, dev, layers=None, x_seed: int = 77):
+        self.nf4, self.wl, self.m, self.dev = nf4, wl, m, dev
+        self.layers = layers if layers is not None else build_layers(nf4, synth, wl, dev)
+        nl = len(self.layers)
+        self.xs = {k: synth.device_activations_bf16(x_seed + k + 1000 * m, m, k, dev) for k in {l.k for l in wl.linears}}
+        self.y_flat = torch.empty(nl * m * sum(lin.n for lin in wl.linears), dtype=torch.bfloat16, device=dev)
+        self.ys, off = [], 0
+        for mats in self.layers:
+            yl = {}
+            for name, (lin, _, _) in mats.items():
+                yl[name] = self.y_flat[off:off + m * lin.n].view(m, lin.n)
+                off += m * lin.n
+            self.ys.append(yl)
+        self.stream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()  # x is drawn on the default stream
+        with torch.cuda.stream(self.stream):
+            run_pass(nf4, self.layers, self.xs, self.ys, self.stream)  # first call builds the table
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            run_pass(nf4, self.layers, self.xs, self.ys, self.stream)
+        torch.cuda.synchronize()
+        self.launches = nl * len(LAYER_STEPS)
+        self.packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin in wl.linears) * nl
+        self.algo = self.packed + nl * sum(2 * m * lin.k + 2 * m * lin.n for lin in wl.linears)
+        self.flops = 2.0 * m * sum(lin.n * lin.k for lin in wl.linears) * nl
+
+    def time(self, steps, warmup):
+        per, total, samples = timed_replays(self.graph, self.stream, steps, warmup, self.dev.index)
+        check_device_error(self.nf4, f"{self.wl.name} M={self.m}")
+        return per, total, samples
+
+    def e2e(self, steps, warmup):
+        """The same graph with every x copied in from pinned host memory and all y copied back each
+        step (the host side of a real decode step).  Returns (seconds per step, h2d, d2h bytes)."""
+        xs_host = {k: v.cpu().pin_memory() for k, v in self.xs.items()}
+        y_host = torch.empty(self.y_flat.shape, dtype=self.y_flat.dtype).pin_memory()
+
+        def step():
+            for k, h in xs_host.items():
+                self.xs[k].copy_(h, non_blocking=True)
+            self.graph.replay()
+            y_host.copy_(self.y_flat, non_blocking=True)
+
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                step()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        check_device_error(self.nf4, f"{self.wl.name} M={self.m} end to end")
+        return e0.elapsed_time(e1) / 1e3 / steps, sum(2 * v.numel() for v in self.xs.values()), 2 * self.y_flat.numel()
+
+
+M1_KERNEL = "gemv_kernel (CUDA-core GEMV, M <= 4) / narrow_kernel<1> (tcgen05, K past the GEMV's range)"
+
+
+def decode_line(dp: DecodePass, steps, warmup, pk):
+    per, total, samples = dp.time(steps, warmup)
+    t = total / steps
+    gbs = dp.packed / t / 1e9
+    return {"workload": dp.wl.name.split(",")[0] + f", M={dp.m}", "M": dp.m, "layers": len(dp.layers),
+            "launches_per_step": dp.launches, "packed_bytes_per_step": dp.packed, "ms_per_step": round(t * 1e3, 4),
+            "packed_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "tflops": round(dp.flops / t / 1e12, 3), "kernel": M1_KERNEL if dp.m <= 4 else "narrow_kernel<8> (tcgen05)",
+            "clocks": clocks_summary(samples)}
+
+
+def single_2048(nf4, synth, dev, pk, steps, warmup):
+    """The single 2048 x 2048 linear at M = 1.  Its 2.2 MB of weights fit in L2, so the timed graph
+    runs it over distinct copies rotating through more than four L2 sizes of memory (cold, the
+    figure reported); the same graph over one copy gives the hot-L2 figure, labelled apart."""
+    wl = W.SINGLE_2048
+    lin = wl.linears[0]
+    w = synth.device_weights(wl.seed * 100003, lin.n, lin.k, dev)
+    codes, scales = nf4.quantize(w)
+    del w
+    packed = lin.n * (lin.k // 2 + lin.k // 64 * 2)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(4, -(-4 * l2 // packed))
+    cs = [(codes.clone(), scales.clone()) for _ in range(copies)]
+    x = synth.device_activations_bf16(1000, 1, lin.k, dev)
+    y = torch.empty((1, lin.n), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    torch.cuda.synchronize()  # x is drawn on the default stream
+    torch.cuda.synchronize()
+    out = {}
+    for label, seq in (("rotated", cs), ("hot_l2", [cs[0]] * copies)):
+        with torch.cuda.stream(stream):
+            for c, s in seq[:2]:
+                nf4.nf4_linear(x, c, s, y, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c, s in seq:
+                nf4.nf4_linear(x, c, s, y, stream)
+        per, total, samples = timed_replays(g, stream, max(3, steps // 20), warmup, dev.index)
+        check_device_error(nf4, f"single 2048 {label}")
+        t = total / max(3, steps // 20) / copies
+        gbs = packed / t / 1e9
+        out[label] = {"us_per_linear": round(t * 1e6, 3), "packed_gbs": round(gbs, 1),
+                      "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "clocks": clocks_summary(samples)}
+    del cs
+    return {"workload": wl.name, "copies": copies, "bytes_rotated": copies * packed, "l2_bytes": l2,
+            "kernel": "gemv_kernel<1,1,2> (CUDA-core GEMV)", "packed_bytes": packed,
+            "figure": "rotated (cold: distinct copies over > 4 x L2); hot_l2 is one copy replayed", **out}
 
-    def step():
-        for mats, yl in zip(layers, ys):
-            for names in LAYER_STEPS:
+
+def prefill_lines(nf4, synth, dev, pk, steps, warmup):
+    """TFLOP/s of the four 20B-shaped prefill linears (gate|up grouped) at M = 32 and M = 512."""
+    wl = W.PREFILL_20B
+    layers = build_layers(nf4, synth, wl, dev)
+    mats = layers[0]
+    out = {}
+    stream = torch.cuda.Stream(device=dev)
+    groups = (("gate", "up"), ("down",), ("qkv",))
+    for m in wl.tokens:
+        xs = {k: synth.device_activations_bf16(99 + k, m, k, dev) for k in {l.k for l in wl.linears}}
+        ys = {name: torch.empty((m, lin.n), dtype=torch.bfloat16, device=dev) for name, (lin, _, _) in mats.items()}
+        torch.cuda.synchronize()  # weights and x are made on the default stream
+
+        def step():
+            for names in groups:
                 lin = mats[names[0]][0]
-                if len(names) == 1:
-                    nf4.nf4_linear(xs[lin.k], mats[names[0]][1], mats[names[0]][2], yl[names[0]], stream)
-                else:
-                    nf4.nf4_linear_grouped(xs[lin.k], [mats[n][1] for n in names], [mats[n][2] for n in names],
-                                           [yl[n] for n in names], stream)
+                nf4.nf4_linear_grouped(xs[lin.k], [mats[n][1] for n in names], [mats[n][2] for n in names],
+                                       [ys[n] for n in names], stream)
 
-    launches = wl.layers * len(LAYER_STEPS)
-    with torch.cuda.stream(stream):
-        step()  # the first call per device builds its constant table, outside the capture
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    torch.cuda.synchronize()
-
-    packed = wl.packed_bytes_per_pass()
-    algo = packed + wl.layers * sum(2 * lin.k + 2 * lin.n for lin in wl.linears)  # + x reads, y writes
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    times, total_s, samples = timed_replays(graph, stream, args.steps, args.warmup, dev.index)
-    if world > 1:
-        torch.distributed.barrier()
-        total_s = max_over_ranks(total_s, dev)
-    clocks = clocks_summary(samples)
-    step_s = statistics.median(times)
-    gbs = job_throughput(packed, args.steps, world, total_s) / 1e9
-    per_launch_s = total_s / args.steps / launches
-    achieved = (algo / launches) / per_launch_s / 1e9
-
-    # end to end: pinned host x in and every y out each step (one transfer of the flat y buffer),
-    # around the same graph of C-ABI calls
-    xs_host = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    y_host = torch.empty(y_flat.shape, dtype=y_flat.dtype).pin_memory()
-
-    def e2e_step():
-        for k, h in xs_host.items():
-            xs[k].copy_(h, non_blocking=True)
-        graph.replay()
-        y_host.copy_(y_flat, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 50))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3 / e2e_steps
-    h2d = sum(2 * k for k in xs_host)
-    d2h = 2 * y_flat.numel()
-
-    prefill = prefill_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
-    embed = embed_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
-    codec = codec_bench(nf4, synth, dev, pk) if not args.skip_prefill else None
-    overflow = overflow_bench(nf4, synth, dev) if not args.skip_prefill else None
-
-    result = {
-        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "launches_per_step": launches,
-                   "launch_structure": "per layer: q|k|v grouped, o, gate|up grouped, down (PDL-chained)",
-                   "packed_bytes_per_step": packed,
-                   "l2": "inputs larger than L2 (1.47 GB of packed weights per step)",
-                   "graph": "one CUDA graph per step", "peak_source": pk["source"]},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": decode_traffic_per_launch(),
-                     "algorithmic_bytes_per_launch": int(algo / launches),
-                     "kernel": "gemv_kernel<1,1,2|4> (CUDA-core GEMV, M = 1)",
-                     "note": "algorithmic bytes (codes+scales+x+y) per launch / average launch time over the "
-                             "timed steps, inter-launch gaps included; peak of measured"},
-        "e2e": {"value": round(packed / e2e_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches * args.steps,
-        "clocks": clocks,
-    }
-    if prefill is not None:
-        result["prefill"] = prefill
-    if embed is not None:
-        result["embed"] = embed
-    if codec is not None:
-        result.update(codec)  # "quantize" and "dequant"
-    if overflow is not None:
-        result["overflow"] = overflow
-    return result
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        n = max(10, steps // 4)
+        times, total, samples = timed_replays(graph, stream, n, warmup, dev.index)
+        check_device_error(nf4, f"prefill M={m}")
+        t = total / n
+        flops = sum(2.0 * m * lin.n * lin.k for lin, _, _ in mats.values())
+        tf = flops / t / 1e12
+        packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, _, _ in mats.values())
+        out[f"M{m}"] = {"workload": f"20B-shaped prefill, 4 linears, M={m}", "tflops": round(tf, 2),
+                        "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                        "frac_of_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4),
+                        "peak_note": "burst peak: a sub-millisecond graph replayed; sustained beside it",
+                        "kernel": "narrow_kernel<32> (tcgen05, small M)" if m <= 32 else
+                                  "stream_kernel<256> (tcgen05 GEMM, dequant into tensor memory)",
+                        "packed_gbs": round(packed / t / 1e9, 1), "frac_of_hbm": round(packed / t / 1e9 / pk["hbm_gbs"], 4),
+                        "ms": round(t * 1e3, 4), "clocks": clocks_summary(samples)}
+    return out
 
 
 def overflow_bench(nf4, synth, dev, layers: int = 2, passes: int = 8):
@@ -296,6 +365,7 @@ def overflow_bench(nf4, synth, dev, layers: int = 2, passes: int = 8):
             samples.append(sample_clocks(dev.index))
         torch.cuda.synchronize()
         ring_s = e0.elapsed_time(e1) / 1e3 / passes
+        check_device_error(nf4, "overflow ring")
     finally:
         ring.close()
     # the link alone: one pinned buffer of the same size copied to the device
@@ -343,6 +413,7 @@ def embed_bench(nf4, synth, dev, pk, vocab: int = 151936, hidden: int = 2048, n_
     while not evs[-1][1].query():
         samples.append(sample_clocks(dev.index))
     torch.cuda.synchronize()
+    check_device_error(nf4, "embed")
     t = statistics.median(a.elapsed_time(b) / 1e3 for a, b in evs)
     algo = n_ids * (4 + hidden // 2 + hidden // 64 * 2 + 2 * hidden)
     gbs = algo / t / 1e9
@@ -389,93 +460,209 @@ def codec_bench(nf4, synth, dev, pk, n: int = 16384, k: int = 16384):
     return out
 
 
-def prefill_bench(nf4, synth, dev, pk):
-    """TFLOP/s of the four 20B-shaped prefill linears (gate|up grouped) at M = 32 and M = 512."""
-    wl = W.PREFILL_20B
-    mats = {}
-    for li, lin in enumerate(wl.linears):
-        w = synth.device_weights(wl.seed * 100003 + li, lin.n, lin.k, dev, outlier_frac=wl.outlier_frac)
-        mats[lin.name] = (lin,) + tuple(nf4.quantize(w))
-        del w
-    out = {}
-    stream = torch.cuda.Stream(device=dev)
-    groups = (("gate", "up"), ("down",), ("qkv",))
-    for m in wl.tokens:
-        xs = {k: synth.device_activations_bf16(99 + k, m, k, dev) for k in {l.k for l in wl.linears}}
-        ys = {name: torch.empty((m, lin.n), dtype=torch.bfloat16, device=dev) for name, (lin, _, _) in mats.items()}
-        torch.cuda.synchronize()  # weights and x are made on the default stream
-
-        def step():
-            for names in groups:
-                lin = mats[names[0]][0]
-                nf4.nf4_linear_grouped(xs[lin.k], [mats[n][1] for n in names], [mats[n][2] for n in names],
-                                       [ys[n] for n in names], stream)
-
-        with torch.cuda.stream(stream):
-            step()
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-        times, _, samples = timed_replays(graph, stream, 50, 5, dev.index)
-        t = statistics.median(times)
-        flops = sum(2.0 * m * lin.n * lin.k for lin, _, _ in mats.values())
-        tf = flops / t / 1e12
-        packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, _, _ in mats.values())
-        out[f"M{m}"] = {"tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-                        "frac_of_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4),
-                        "peak_note": "burst peak: 50 replays of a sub-millisecond graph; sustained beside it",
-                        "kernel": f"stream_kernel<{32 if m <= 32 else 256}> (tcgen05, dequant into tensor memory)",
-                        "packed_gbs": round(packed / t / 1e9, 1), "ms": round(t * 1e3, 4),
-                        "clocks": clocks_summary(samples)}
-    return out
-
-
 # ------------------------------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and --impl reference)
 # ------------------------------------------------------------------------------------------------
-def oracle_sample(seconds_budget: float = 15.0):
-    """Time the oracle's fp64 linear on one 3B-shaped layer (7 linears, M = 1) and express it as
-    packed GB/s.  Returns (GB/s, threads, description)."""
-    import oracle
+def oracle_layer_sample(o, seed: int = 5):
+    """One 32B-shaped layer (7 linears, M = 1) of random packed weights drawn on the host (the
+    oracle's speed does not depend on the values), with x from the seeded generator."""
     from nf4_weight_only_gb300 import synth
-    o = oracle.default()
-    wl = W.DECODE_3B
-    threads = os.cpu_count() or 1
-    prepared = []
-    for li, lin in enumerate(wl.linears):
-        w = synth.weights(wl.seed * 100003 + li, lin.n, lin.k)
-        codes, scales = o.quantize(w)
-        prepared.append((lin, codes, scales, synth.activations_bf16(77 + lin.k, 1, lin.k)))
-    packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, *_ in prepared)
+    rng = np.random.default_rng(seed)
+    out = []
+    for lin in HEADLINE.linears:
+        codes = rng.integers(0, 256, size=(lin.n, lin.k // 2), dtype=np.uint8)
+        scales = (rng.random((lin.n, lin.k // 64), dtype=np.float32) * 0.09 + 0.01).astype(np.float16).view(np.uint16)
+        out.append((lin, codes, scales, synth.activations_bf16(seed + lin.k, 1, lin.k)))
+    return out
+
+
+def time_oracle(o, sample, threads: int, budget_s: float, max_reps: int = 50):
+    """Repeat the oracle's fp64 linear over `sample` until `budget_s` seconds have passed.
+    Returns (packed GB/s, seconds, repetitions)."""
+    packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, *_ in sample)
     reps, total = 0, 0.0
-    while total < seconds_budget and reps < 50:
+    while (total < budget_s or reps == 0) and reps < max_reps:
         t0 = time.perf_counter()
-        for lin, codes, scales, x in prepared:
+        for lin, codes, scales, x in sample:
             o.linear(x, codes, scales, nthreads=threads)
         total += time.perf_counter() - t0
         reps += 1
-    gbs = packed * reps / total / 1e9
-    return gbs, threads, (f"{reps} pass(es) over one 3B-shaped layer (7 linears, {packed / 1e6:.1f} MB packed), "
-                          f"M=1, fp64 oracle, {threads} threads")
+    return packed * reps / total / 1e9, total, reps
+
+
+def cpu_baseline(o):
+    """The oracle on this host's cores: all threads on a whole 32B-shaped layer, one thread on its q
+    projection (a rate in the metric's unit; nothing is extrapolated)."""
+    threads = os.cpu_count() or 1
+    sample = oracle_layer_sample(o)
+    gbs, secs, reps = time_oracle(o, sample, threads, 8.0)
+    gbs1, secs1, reps1 = time_oracle(o, sample[:1], 1, 4.0)
+    lin = sample[0][0]
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{reps} pass(es) over one 32B-shaped layer (7 linears, 259 MB packed, random codes), "
+                       f"M=1, fp64 oracle, {threads} threads, {secs:.2f} s measured"),
+            "extrapolated": False,
+            "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps1} pass(es) over the {lin.k}->{lin.n} q projection, {secs1:.2f} s measured"}}
+
+
+def check_sampled_outputs(nf4, o, dp: DecodePass, checks=((0, "q"), (0, "gate"), (-1, "down")), rows_per: int = 64,
+                          seed: int = 7):
+    """Sampled outputs of the timed graph against the oracle: for the listed (layer, linear) pairs,
+    the same fp32 weights are drawn again on the device, the sampled rows copied to the host and
+    quantized by the oracle (which must give the GPU's codes and scales bit for bit), and the oracle's
+    linear on those codes and the generator's x must bound the GPU's outputs."""
+    from nf4_weight_only_gb300 import synth
+    wl = dp.wl
+    rng = np.random.default_rng(seed)
+    names = [lin.name for lin in wl.linears]
+    worst, checked = 0.0, 0
+    for layer, name in checks:
+        layer = layer % len(dp.layers)
+        li = names.index(name)
+        lin, codes_d, scales_d = dp.layers[layer][name]
+        rows = np.unique(np.concatenate([[0, lin.n - 1], rng.choice(lin.n, rows_per - 2, replace=False)]))
+        w = synth.device_weights(wl.seed * 100003 + layer * 16 + li, lin.n, lin.k, dp.dev, outlier_frac=wl.outlier_frac)
+        sel = torch.from_numpy(rows.astype(np.int64)).to(dp.dev)
+        w_rows = w[sel].cpu().numpy()
+        del w
+        c_ref, s_ref = o.quantize(w_rows)
+        if not (np.array_equal(codes_d[sel].cpu().numpy(), c_ref) and
+                np.array_equal(scales_d[sel].cpu().view(torch.int16).numpy().view(np.uint16), s_ref)):
+            raise BenchError(f"layer {layer} {name}: packed weights differ from the oracle's")
+        x = dp.xs[lin.k].cpu().view(torch.int16).numpy().view(np.uint16)
+        y64, mag = o.linear(x, c_ref, s_ref, nthreads=os.cpu_count() or 1)
+        got = dp.ys[layer][name].cpu().view(torch.int16).numpy().view(np.uint16)[:, rows]
+        import oracle as oracle_mod
+        ok, ratio, mask = oracle_mod.within_tolerance(got, y64, mag)
+        if not ok:
+            raise BenchError(f"layer {layer} {name}: {np.count_nonzero(~mask)} sampled outputs outside the bound")
+        worst = max(worst, float(ratio))
+        checked += got.size
+    return {"outputs_checked": int(checked), "worst_error_over_bound": round(worst, 4), "ok": True,
+            "linears": [f"layer {l % len(dp.layers)} {n}" for l, n in checks]}
 
 
 def run_reference(args, rank, world):
+    """The oracle, as it stands, on this host's cores; a step is one 32B-shaped layer (7 linears) of
+    the headline pass, timed in full."""
     if rank != 0:
         return None
-    budget = max(5.0, min(60.0, 0.05 * args.steps + 5.0))
-    gbs, cores, sample = oracle_sample(budget)
-    wl = W.DECODE_3B
-    step_s = wl.packed_bytes_per_pass() / (gbs * 1e9)
+    import oracle
+    o = oracle.default()
+    threads = os.cpu_count() or 1
+    sample = oracle_layer_sample(o)
+    packed = sum(lin.n * (lin.k // 2 + lin.k // 64 * 2) for lin, *_ in sample)
+    for _ in range(args.warmup):
+        time_oracle(o, sample, threads, 0.0, max_reps=1)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        time_oracle(o, sample, threads, 0.0, max_reps=1)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    gbs = packed * args.steps / total / 1e9
     return {
         "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "config": {"workload": HEADLINE.name, "step": "one layer (7 linears, 259 MB packed) of the 64-layer pass, timed in full"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} steps of one 32B-shaped layer, fp64 oracle, {threads} threads, "
+                                   f"{total:.2f} s measured", "extrapolated": False},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def run_ours(args, rank, world):
+    import nf4_weight_only_gb300 as nf4
+    from nf4_weight_only_gb300 import build, synth
+
+    build.build()
+    nf4.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    only = set(args.only.split(",")) if args.only else None
+
+    def want(name):
+        return only is None or name in only
+
+    result = {}
+    if want("headline"):
+        dp = DecodePass(nf4, synth, HEADLINE, 1, dev,
+                        layers=build_layers(nf4, synth, HEADLINE, dev, layers=args.layers), x_seed=377)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        per, total_s, samples = dp.time(args.steps, args.warmup)
+        if world > 1:
+            torch.distributed.barrier()
+            total_s = max_over_ranks(total_s, dev)
+        step_s = statistics.median(per)
+        gbs = job_throughput(dp.packed, args.steps, world, total_s) / 1e9
+        per_launch_s = total_s / args.steps / dp.launches
+        achieved = (dp.algo / dp.launches) / per_launch_s / 1e9
+        e2e_s, h2d, d2h = dp.e2e(max(3, min(args.steps, 50)), max(3, args.warmup))
+        result = {
+            "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": HEADLINE.name if args.layers is None else f"{HEADLINE.name} (first {args.layers} layers)",
+                       "M": 1, "launches_per_step": dp.launches,
+                       "launch_structure": "per layer: q|k|v grouped, o, gate|up grouped, down (PDL-chained)",
+                       "packed_bytes_per_step": dp.packed,
+                       "l2": f"inputs larger than L2 ({dp.packed / 1e9:.2f} GB of packed weights per step)",
+                       "graph": "one CUDA graph per step", "peak_source": pk["source"]},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": traffic_per_launch("gemv_decode_32b_launch_list.md"),
+                         "algorithmic_bytes_per_launch": int(dp.algo / dp.launches), "kernel": M1_KERNEL,
+                         "note": "algorithmic bytes (codes+scales+x+y) per launch / average launch time over the "
+                                 "timed steps, inter-launch gaps included; peak of measured"},
+            "packed_frac_of_hbm": round(gbs / world / pk["hbm_gbs"], 4),
+            "e2e": {"value": round(dp.packed / e2e_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": dp.launches * args.steps,
+            "clocks": clocks_summary(samples),
+        }
+        if rank == 0 and not args.skip_cpu_baseline:
+            import oracle
+            o = oracle.default()
+            result["cpu_baseline"] = cpu_baseline(o)
+            result["output_check"] = check_sampled_outputs(nf4, o, dp)
+        del dp
+        torch.cuda.empty_cache()
+    configs = {}
+    steps_sub, warm_sub = max(5, args.steps // 2), max(3, args.warmup)
+    if want("c1"):
+        configs["single_2048"] = single_2048(nf4, synth, dev, pk, args.steps, warm_sub)
+    if want("c2"):
+        dp = DecodePass(nf4, synth, W.DECODE_3B, 1, dev)
+        configs["decode_3b_M1"] = decode_line(dp, steps_sub, warm_sub, pk)
+        del dp
+        torch.cuda.empty_cache()
+    if want("c3"):
+        layers = build_layers(nf4, synth, W.DECODE_14B, dev)
+        for m in W.DECODE_14B.tokens:
+            dp = DecodePass(nf4, synth, W.DECODE_14B, m, dev, layers=layers, x_seed=177)
+            configs[f"decode_14b_M{m}"] = decode_line(dp, steps_sub, warm_sub, pk)
+            del dp
+        del layers
+        torch.cuda.empty_cache()
+    if want("c5"):
+        for k, v in prefill_lines(nf4, synth, dev, pk, steps_sub, warm_sub).items():
+            configs[f"prefill_20b_{k}"] = v
+        torch.cuda.empty_cache()
+    if configs:
+        result["configs"] = configs
+    if want("codec"):
+        result.update(codec_bench(nf4, synth, dev, pk))
+    if want("embed"):
+        result["embed"] = embed_bench(nf4, synth, dev, pk)
+    if want("overflow"):
+        result["overflow"] = overflow_bench(nf4, synth, dev)
+    return result
 
 
 def profile_linear(m: int, n: int, k: int) -> None:
@@ -514,10 +701,13 @@ def profile_codec(n: int, k: int) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill, embedding, codec and overflow lines")
+    ap.add_argument("--only", default=None,
+                    help="comma-separated subset of headline,c1,c2,c3,c5,codec,embed,overflow (default: all)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers of the headline workload (for profiler captures)")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--profile-codec", nargs=2, type=int, metavar=("N", "K"),
                     help="quantize and dequantize one N x K matrix (for single-kernel profiler captures)")
@@ -540,13 +730,13 @@ def main():
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if True:
+    try:
         res = run_ours(args, rank, world)
-        if rank == 0 and res is not None and not args.skip_cpu_baseline:
-            gbs, cores, sample = oracle_sample(15.0)
-            res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                   "sample": sample}
-    if rank == 0 and res is not None:
+    except BenchError as e:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": None, "error": str(e)}))
+        sys.exit(1)
+    if rank == 0 and res:
         print(json.dumps(res))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -97,8 +97,8 @@ nf4_status nf4_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, 
 /*
  * nf4_linear - y = x * w_hat^T with the weights streamed in packed form and dequantized tile by
  * tile on chip (deep-fold README, execution-path table: N=1 decode GEMV, prefill GEMM of up to 32
- * positions; larger M is this library's extension).  M <= 4 runs a CUDA-core GEMV (K up to 32768
- * for M = 1, 16384 for M = 2..4); M <= 32, and M <= 4 with a longer K, run a weight-streaming
+ * positions; larger M is this library's extension).  M <= 3 runs a CUDA-core GEMV (K up to 32768
+ * for M = 1, 16384 for M = 2..3); M <= 32, and M <= 3 with a longer K, run a weight-streaming
  * kernel that dequantizes on the CUDA cores into tensor memory and multiplies on the tcgen05 tensor
  * cores (one CTA per SM, K split into slices when a CTA has few rows); larger M runs a tcgen05 GEMM
  * over 128-row weight tiles.  The kernel depends on M and K; the K split on M, N and the SM count.

@@ -1,4 +1,4 @@
-// NF4 GEMV family on CUDA cores (sm_103a): y[M, N] = x[M, K] * w_hat[N, K]^T for 1 <= M <= 4.
+// NF4 GEMV family on CUDA cores (sm_103a): y[M, N] = x[M, K] * w_hat[N, K]^T for 1 <= M <= 3.
 //
 // Decode is weight streaming (deep-fold README, execution-path table: the N=1 decode step runs a
 // GEMV on CUDA cores and dequantizes only the current tile).  The kernel's job is to consume the
@@ -811,7 +811,6 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
                                    : launch_gemv_t<1, 1, 2>(x, P, K, num_sms, stream);
         case 2: return launch_gemv_t<2, 2, 2>(x, P, K, num_sms, stream);
         case 3: return launch_gemv_t<3, 2, 2>(x, P, K, num_sms, stream);
-        case 4: return launch_gemv_t<4, 2, 2>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -161,23 +161,30 @@ def _layers_14b(nf4):
 
 
 def test_sweep_32b_pass(nf4, o):
-    """32B-shaped sweep (64 layers, 16.6 GB packed, M = 1): layers 0 and 63 checked on 256 rows of
-    each linear, every other layer on 4."""
+    """32B-shaped sweep (64 layers, 16.6 GB packed, M = 1), the bench's headline: its 256 PDL-chained
+    launches captured in one CUDA graph and replayed; layers 0 and 63 checked on 256 rows of each
+    linear, every other layer on 4."""
     from nf4_weight_only_gb300 import synth, workloads as W
     _cache.clear()
     torch.cuda.empty_cache()
     wl = W.SWEEP_32B
     layers = bench.build_layers(nf4, synth, wl, DEV)
-    xs = {k: synth.device_activations_bf16(377 + k, 1, k, DEV) for k in {l.k for l in wl.linears}}
-    ys = _empty_outputs(layers, 1)
+    xs = {k: synth.device_activations_bf16(377 + k + 1000, 1, k, DEV) for k in {l.k for l in wl.linears}}
     stream = torch.cuda.Stream(device=DEV)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
+        _run_pass(nf4, layers, xs, _empty_outputs(layers, 1), stream)
+    torch.cuda.synchronize()
+    ys = _empty_outputs(layers, 1)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
         _run_pass(nf4, layers, xs, ys, stream)
+    graph.replay()
+    graph.replay()
     torch.cuda.synchronize()
     assert _device_error(nf4) == 0
     _check_pass(nf4, o, wl, layers, xs, ys, {0, wl.layers - 1}, 256, 4, seed=64)
-    del layers
+    del layers, graph
     torch.cuda.empty_cache()
 
 
