@@ -235,7 +235,7 @@ class DecodePass:
         return e0.elapsed_time(e1) / 1e3 / steps, sum(2 * v.numel() for v in self.xs.values()), 2 * self.y_flat.numel()
 
 
-M1_KERNEL = "gemv_kernel (CUDA-core GEMV, M <= 4) / narrow_kernel<1> (tcgen05, K past the GEMV's range)"
+M1_KERNEL = "gemv_kernel (CUDA-core GEMV, M <= 3) / narrow_kernel<1> (tcgen05, K past the GEMV's range)"
 
 
 def decode_line(dp: DecodePass, steps, warmup, pk):

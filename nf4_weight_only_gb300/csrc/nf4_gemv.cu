@@ -806,9 +806,16 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
     P.row0[count] = static_cast<int>(rows);
     for (int i = count + 1; i <= kMaxGroup; i++) P.row0[i] = P.row0[count];
     switch (M) {
-        case 1:  // K past one slice (32 groups): four rows per warp, else up to two
-            return K > 32 * kGroup ? launch_gemv_t<1, 1, 4>(x, P, K, num_sms, stream)
-                                   : launch_gemv_t<1, 1, 2>(x, P, K, num_sms, stream);
+        case 1: {
+            // K past one slice (32 groups): four rows per warp, else up to two.  Past one slice,
+            // two lanes per group (slices of 16 groups) when that leaves fewer lanes idle: K = 5120
+            // is 80 groups, three slices of 32 with 16 lanes idle, or five full slices of 16.
+            if (K <= 32 * kGroup) return launch_gemv_t<1, 1, 2>(x, P, K, num_sms, stream);
+            const int64_t G = K / kGroup;
+            const int64_t s1 = (G + 31) / 32, s2 = (G + 15) / 16;
+            if (s2 <= kMaxWarps && 16 * s2 < 32 * s1) return launch_gemv_t<1, 2, 4>(x, P, K, num_sms, stream);
+            return launch_gemv_t<1, 1, 4>(x, P, K, num_sms, stream);
+        }
         case 2: return launch_gemv_t<2, 2, 2>(x, P, K, num_sms, stream);
         case 3: return launch_gemv_t<3, 2, 2>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;

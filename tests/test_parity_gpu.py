@@ -186,6 +186,14 @@ def test_linear_k27648_m1(nf4, o):
     check_linear(nf4, o, 1, 160, 27648, seed=5)
 
 
+@pytest.mark.parametrize("n,k", [(1000, 2112), (4099, 5120), (513, 3072), (700, 11008), (3000, 15360)])
+def test_linear_m1_two_lanes_per_group(nf4, o, n, k):
+    """M = 1 where two lanes per group leave fewer lanes idle than one (33, 80, 48, 172 and 240
+    groups; 240 is 15 slices of 16, one short of the most a CTA holds): whole slices, a slice with
+    a single group, several row blocks per CTA."""
+    check_linear(nf4, o, 1, n, k, seed=n + 3 * k)
+
+
 def test_linear_m33_outliers(nf4, o):
     check_linear(nf4, o, 33, 130, 6144, seed=6, outliers=0.01)
 
