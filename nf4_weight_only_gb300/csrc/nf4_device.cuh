@@ -190,6 +190,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Non-blocking test of phase `parity` (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for a warp that spends most of its time waiting off the critical path (a producer
+// whose ring is full, a reducer waiting for the consumers).  A blocking try_wait keeps the waiting
+// warp issuing retries, which on this GPU takes issue slots from the warps that share its
+// scheduler; this wait tests without blocking and sleeps `sleep_ns` between tests instead, at the
+// cost of up to about that much wake-up latency.  Same result and limit rule as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, uint64_t limit_ns, uint32_t sleep_ns) {
+    if (mbar_ready(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 1;; n++) {
+        __nanosleep(sleep_ns);
+        if (mbar_ready(bar, parity)) return true;
+        if ((n & 7) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // One lane of a converged warp (the same lane on every call) is true.  tcgen05.mma, tcgen05.commit
 // and the TMA copies are issued by a single thread, but the warp around it runs the issue loop in
 // step: its operands then stay warp-uniform, which lets each instruction issue in tens of cycles

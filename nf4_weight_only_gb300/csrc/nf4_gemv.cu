@@ -4,18 +4,17 @@
 // GEMV on CUDA cores and dequantizes only the current tile).  The kernel's job is to consume the
 // packed codes at HBM speed, which leaves about three to four issue slots per weight on a GB300.
 //
-// Scale factorisation.  A nonzero fp16 scale is 2^E * (1 + m/1024) with m its top ten fraction
-// bits (fp16 subnormals included, read as binary32).  Rounding commutes with multiplication by a
-// power of two, so w_hat = bf16(fp32(T[c] * scale)) = 2^E * V[m][c] with V[m][c] =
-// bf16(fp32(T[c] * (1 + m/1024))).  V is a 1024 x 16 bf16 table built once per device.  A lane sums
-// x_k * V[m][c_k] over its group in fp32 (each bf16 x bf16 product is exact) and scales the group
-// sum by 2^E, which is exact too: the result equals the sum of x_k * w_hat_k in that order.
-//
-// Lookup.  Per (row, group) a lane holds its V row as eight registers: the low bytes and the high
-// bytes of the 16 bf16 entries, each split into codes 0-7 and 8-15.  `prmt` reads a 4-bit code
-// nibble as a byte selector, so one instruction looks up one byte plane for four codes; a
-// sign-replicating `prmt` turns bit 3 of each code into a byte mask that picks the 0-7 or the 8-15
-// half.  Eight weights cost 22 integer instructions before the multiply-adds.
+// Dequantization.  The GEMV computes w_hat = bf16(fp32(T[c] * scale)) as the definition states,
+// two weights at a time: a code byte (two codes) indexes a 256-entry shared-memory table whose
+// entry is the fp32 pair {T[low nibble], T[high nibble]}; one packed fp32x2 multiply by the group's
+// scale (round to nearest) and one bf16x2 conversion (round to nearest even) give both weights.
+// The table is replicated across the 32 lanes (entry v, lane l at byte 256 v + 8 l), so a warp's
+// 64-bit loads hit 32 distinct bank pairs per half-warp whatever the codes are; one byte permute
+// builds that address from the code word.  Eight weights cost 4 permutes, 4 shared loads, 4 packed
+// multiplies and 4 conversions before the multiply-adds: the loop is bound by shared-memory
+// bandwidth (8 bytes per 2 weights), about 1.4 times the rate of a 16-entry register lookup done
+// with byte permutes, which is bound by the integer pipe.  A lane sums x_k * w_hat_k in fp32 (each
+// bf16 x bf16 product is exact).
 //
 // Work layout.  A warp owns a K-slice (32 groups at one lane per group, or 16 groups at two lanes
 // per group) and keeps that slice of x in registers as bf16 pairs; it streams four rows at a time
@@ -36,15 +35,21 @@ namespace {
 constexpr int kMaxWarps = 16;  // consumer warps per CTA (slices x row lanes)
 constexpr int kHalfWarps = 8;  // consumer warps of a CTA that leaves room for a second one
 constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
-constexpr int kVtabBytes = 1024 * 32;  // V table copy in shared memory
+constexpr int kPairTabBytes = 256 * 32 * 8;  // code-byte table, one 8-byte column per lane (64 KB)
 
-// V table.  Row R holds the 16 bf16 entries of one scale class as two 16-byte chunks: the low bytes
+// V table (the tensor-core kernels' dequantization, which writes bf16 operands rather than
+// multiply-adds).  Scale factorisation: a nonzero fp16 scale is 2^E * (1 + m/1024) with m its top ten
+// fraction bits (fp16 subnormals included, read as binary32).  Rounding commutes with multiplication
+// by a power of two, so w_hat = bf16(fp32(T[c] * scale)) = 2^E * V[m][c] with V[m][c] =
+// bf16(fp32(T[c] * (1 + m/1024))).  Per (row, group) a lane holds its V row as eight registers (low
+// and high byte planes, codes 0-7 and 8-15), and `prmt` looks up one byte plane for four codes.
+// Row R holds the 16 bf16 entries of one scale class as two 16-byte chunks: the low bytes
 // {L(0..3), L(4..7), L(15..12), L(11..8)} at chunk R and the high bytes in the same order at chunk
 // kVtabHi + R, L / H being the low / high byte of the entry for code c.  Codes 8..15 are stored in
 // reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.
-// Rows 0..1023 hold V[m][c] = bf16(fp32(T[c] * (1 + m/1024))); rows 1024..2047 hold 2 * V[m][c] (the
-// same values one binade up, exact); row 2048 is all zeros.  The GEMV and the GEMM-form streaming
-// kernel read rows 0..1023; the small-M streaming kernel reads all of them.
+// Rows 0..1023 hold V[m][c]; rows 1024..2047 hold 2 * V[m][c] (the same values one binade up,
+// exact); row 2048 is all zeros.  The GEMM-form streaming kernel reads rows 0..1023; the small-M
+// streaming kernel reads all of them.
 constexpr int kVtabRows = 2049;
 constexpr int kVtabHi = 2056;                  // first high-byte chunk
 constexpr int kVtabChunks = kVtabHi + 2056;    // 4112 chunks (65,792 bytes)
@@ -70,11 +75,12 @@ __global__ void build_vtab_kernel() {
     g_vtab[kVtabHi + row] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// Shared-memory copy of rows 0..1023 for the GEMV and the GEMM-form kernel: 1024 low-byte chunks,
+// Shared-memory copy of rows 0..1023 for the GEMM-form kernel: 1024 low-byte chunks,
 // then 1024 high-byte chunks (32 KB).  Chunk i of the copy.
 __device__ __forceinline__ const uint4* vtab_src32k(int i) { return &g_vtab[i < 1024 ? i : kVtabHi + (i - 1024)]; }
 
-// Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order.
+// Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order, from a
+// V-table row held in registers (tensor-core kernels).
 // 18 ALU-pipe instructions (PRMT / LOP3) and 4 FMA-pipe ones (selector preparation).
 __device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4& th, uint32_t m1, uint32_t p16,
                                         uint32_t out[4]) {
@@ -91,6 +97,22 @@ __device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4
     hi = select_bits(prmt(th.x, th.y, wh), prmt(th.z, th.w, nwh), msk);
     out[2] = prmt(lo, hi, 0x5140u);
     out[3] = prmt(lo, hi, 0x7362u);
+}
+
+// Two dequantized weights from one code byte: the pair-table entry {T[c0], T[c1]} (fetched by the
+// caller) times the scale in one packed fp32 multiply, then both rounded to bf16 (c0 in the low
+// half).  Equals bf16(fp32(T[c] * scale)) for each code.
+__device__ __forceinline__ uint32_t scale_pair(float2 t, float s) {
+    uint32_t d;
+    asm("{\n\t.reg .b64 t, s2, r;\n\t.reg .f32 p0, p1;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "mov.b64 s2, {%3, %3};\n\t"
+        "mul.rn.f32x2 r, t, s2;\n\t"
+        "mov.b64 {p0, p1}, r;\n\t"
+        "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+        : "=r"(d)
+        : "f"(t.x), "f"(t.y), "f"(s));
+    return d;
 }
 
 // First stage of summing each of V values over the 32 lanes.  Recursive halving: at each of log2(V)
@@ -145,6 +167,10 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_tc_error, 
 // bug, not a slow GPU).  Every wait has its own limit, so no kernel length can exhaust it.
 __device__ unsigned long long g_wait_ns = 1000000000ull;
 
+// Sleep between the tests of the producer's and the reducer's waits (mbar_wait_idle): both wait
+// most of the time, and neither is on the consumers' critical path while the ring has room.
+constexpr uint32_t kIdleSleepNs = 256;
+
 // Per-row metadata the producer writes next to each row's data.
 struct RowMeta {
     int problem;     // index into GemvProblems
@@ -181,7 +207,7 @@ struct GemvLayout {
 template <int MT, int LPG, int RMAX>
 __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K,
-                const GemvLayout L, uint32_t m1, uint32_t p16) {
+                const GemvLayout L) {
     constexpr int WPL = kGroup / LPG;  // weights per consumer lane per row
     constexpr int CB = WPL / 2;        // code bytes per consumer lane per row
     constexpr int CHUNKS = CB / 16;
@@ -195,9 +221,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     const int C = L.S * L.Q;
     const int G = K / kGroup;
     const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    const uint4* vtab = reinterpret_cast<const uint4*>(smem);
-    uint8_t* ring = smem + kVtabBytes;
-    const uint32_t bars = sbase + kVtabBytes + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
+    uint8_t* ring = smem + kPairTabBytes;
+    const uint32_t bars = sbase + kPairTabBytes + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
     // this CTA's rows: a contiguous range, the N rows split as evenly as the grid allows
     const int64_t rbeg = static_cast<int64_t>(N) * blockIdx.x / gridDim.x;
     const int64_t rend = static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x;
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         constexpr int LPV = 32 / V;  // lanes holding one value after the halving steps
         int st = 0, par = 0;
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (2 * L.ST + st), par, wait_ns))) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_idle(bars + 8 * (2 * L.ST + st), par, wait_ns, kIdleSleepNs))) {
                 record_error(13);
                 break;
             }
@@ -260,7 +285,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         // 16-byte copies.  Every row of the block gets its metadata (valid = 0 past the end).
         int st = 0, round = 0;  // ring stage of block t and how often the ring has wrapped
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, round += st == 0) {
-            if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * (L.ST + st), (round - 1) & 1, wait_ns))) {
+            if (round > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait_idle(bars + 8 * (L.ST + st), (round - 1) & 1, wait_ns, kIdleSleepNs))) {
                 record_error(11);
                 break;
             }
@@ -275,7 +300,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 if (r < rend) {
                     const int pp = problem_of(P, r);
                     const int64_t lr = r - P.row0[pp];
-                    bulk_copy_g2s(sbase + static_cast<uint32_t>(kVtabBytes + st * L.stage_bytes + j * L.row_code_bytes),
+                    bulk_copy_g2s(sbase + static_cast<uint32_t>(kPairTabBytes + st * L.stage_bytes + j * L.row_code_bytes),
                                   P.codes[pp] + lr * (K / 2), static_cast<uint32_t>(K / 2), bars + 8 * st);
                     const int64_t sfirst = lr * G * 2;
                     const int64_t a = sfirst & ~static_cast<int64_t>(15);
@@ -306,10 +331,15 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         // Lanes whose bit 2 is set read the two 16-byte halves of their 32 code bytes in the other
         // order (no bank conflicts for eight lanes 32 bytes apart); x is loaded in the same order.
         const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
-        // The V table is for the consumers alone: they copy it while the producer already streams
-        // the first row blocks, and meet on a named barrier before the first lookup.
-        for (int i = threadIdx.x; i < kVtabBytes / 16; i += 32 * C) cp_async16(smem + 16 * i, vtab_src32k(i));
-        cp_async_commit();
+        // The pair table is for the consumers alone: they write it while the producer already streams
+        // the first row blocks, and meet on a named barrier before the first lookup.  Entry e of the
+        // table (byte v = e / 32, lane column e % 32) is warp-uniform in v, so the constant reads
+        // do not diverge.
+        float2* ptab = reinterpret_cast<float2*>(smem);
+        for (int e = threadIdx.x; e < kPairTabBytes / 8; e += 32 * C) {
+            const int v = e >> 5;
+            ptab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
+        }
         pdl_wait();
         uint32_t xr[MT][WPL / 2];
 #pragma unroll
@@ -325,8 +355,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 xr[tt][4 * i + 3] = v.w;
             }
         }
-        cp_async_wait<0>();
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * C) : "memory");  // every consumer's table chunks landed
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * C) : "memory");  // every consumer's table entries written
+        const uint32_t lcol = static_cast<uint32_t>(lane) * 8;  // this lane's column in every table entry
         int st = 0, par = 0;  // ring stage of block t and the phase parity of its barriers
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, wait_ns))) {
@@ -341,10 +371,9 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
             float part[V];
 #pragma unroll
             for (int i = 0; i < V; i++) part[i] = 0.0f;
-            // Row prologues first (metadata -> scale -> table is a chain of dependent shared-memory
-            // loads), for all of this warp's rows of the block, so that their latencies overlap.
-            uint4 tl[RMAX], th[RMAX];
-            float pow2[RMAX];
+            // Row prologues first (metadata -> scale is a chain of dependent shared-memory loads), for
+            // all of this warp's rows of the block, so that their latencies overlap.
+            float scl[RMAX];
             bool rv[RMAX];
 #pragma unroll
             for (int jj = 0; jj < RMAX; jj++) {
@@ -355,11 +384,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 uint32_t sc = 0;
                 if (rv[jj] && active)
                     sc = *reinterpret_cast<const uint16_t*>(stg + L.scales_off + j * L.swin + meta.scale_off + 2 * g);
-                const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(sc))));
-                const uint32_t m = (sb >> 13) & 0x3FFu;
-                pow2[jj] = __uint_as_float(sb & 0xFF800000u);  // +-2^E, or 0 for a zero scale
-                tl[jj] = vtab[m];
-                th[jj] = vtab[1024 + m];
+                scl[jj] = __half2float(__ushort_as_half(static_cast<uint16_t>(sc)));  // exact
             }
 #pragma unroll
             for (int jj = 0; jj < RMAX; jj++) {
@@ -377,18 +402,18 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                     for (int wi = 0; wi < 4; wi++) {
-                        uint32_t wp[4];
-                        lookup8(words[wi], tl[jj], th[jj], m1, p16, wp);
 #pragma unroll
-                        for (int tt = 0; tt < MT; tt++) {
+                        for (int p = 0; p < 4; p++) {
+                            // byte p of the word: table offset 256 * byte + 8 * lane in one permute
+                            const uint32_t off = prmt(words[wi], lcol, 0x6504u + 16u * p);
+                            const uint32_t wp = scale_pair(*reinterpret_cast<const float2*>(smem + off), scl[jj]);
 #pragma unroll
-                            for (int p = 0; p < 4; p++)
-                                fma_bf16x2(a0[tt], a1[tt], wp[p], xr[tt][4 * (4 * c + wi) + p]);
+                            for (int tt = 0; tt < MT; tt++) fma_bf16x2(a0[tt], a1[tt], wp, xr[tt][4 * (4 * c + wi) + p]);
                         }
                     }
                 }
 #pragma unroll
-                for (int tt = 0; tt < MT; tt++) part[jj * MT + tt] = (a0[tt] + a1[tt]) * pow2[jj];
+                for (int tt = 0; tt < MT; tt++) part[jj * MT + tt] = a0[tt] + a1[tt];
             }
             // leave this warp's halved sums in the stage for the reducer
             float* red = reinterpret_cast<float*>(ring + st * L.stage_bytes + L.red_off);
@@ -452,16 +477,16 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     L.meta_off = L.scales_off + L.RB * L.swin;
     L.red_off = L.meta_off + 16 * L.RB;
     L.stage_bytes = L.red_off + L.S * L.Q * 32 * 4;  // one float per consumer lane
-    // ring depth: as many stages as fit next to the V table in the CTA's share of shared memory (at
+    // ring depth: as many stages as fit next to the pair table in the CTA's share of shared memory (at
     // most 8, at least 2; see cap_ring)
-    const int budget = (half ? kHalfSmem : 227 * 1024) - kVtabBytes - 3 * 8 * 8 - 64;
+    const int budget = (half ? kHalfSmem : 227 * 1024) - kPairTabBytes - 3 * 8 * 8 - 64;
     const int64_t blocks_per_cta = ((N + grid64 - 1) / grid64 + L.RB - 1) / L.RB;  // of the largest row range
     L.ST = budget / L.stage_bytes;
     if (L.ST > 8) L.ST = 8;
     if (cap_ring && L.ST > blocks_per_cta) L.ST = static_cast<int>(blocks_per_cta < 2 ? 2 : blocks_per_cta);
     if (L.ST < 2) return cudaErrorInvalidValue;  // a row block does not fit twice
     const int grid = static_cast<int>(grid64);
-    const size_t smem = kVtabBytes + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
+    const size_t smem = kPairTabBytes + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
     static std::once_flag attr_once[64];  // the largest possible request, set once per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -481,7 +506,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, RMAX>, x, P, static_cast<int>(K), L, 0xFFFFFFFFu, 0x10000u);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, RMAX>, x, P, static_cast<int>(K), L);
 }
 
 }  // namespace
