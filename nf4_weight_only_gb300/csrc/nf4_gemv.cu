@@ -115,6 +115,23 @@ __device__ __forceinline__ uint32_t scale_pair(float2 t, float s) {
     return d;
 }
 
+// Writes the pair table (kPairTabBytes at `tab`): slot e holds entry v = e / 32, the fp32 pair
+// {T[v & 15], T[v >> 4]} of code byte v, for lane column e % 32.  Threads `tid` of `nthreads` (a
+// multiple of 32) share the work; a warp's 32 slots belong to one entry, so the constant reads do
+// not diverge.
+__device__ __forceinline__ void build_pair_table(float2* tab, int tid, int nthreads) {
+    for (int e = tid; e < kPairTabBytes / 8; e += nthreads) {
+        const int v = e >> 5;
+        tab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
+    }
+}
+
+// Shared-memory offset of the pair-table entry of byte p (0..3) of a code word for the lane whose
+// column offset is `lcol` (8 * lane): 256 * byte + lcol, built by one byte permute.
+__device__ __forceinline__ uint32_t pair_offset(uint32_t word, uint32_t lcol, int p) {
+    return prmt(word, lcol, 0x6504u + 16u * static_cast<uint32_t>(p));
+}
+
 // First stage of summing each of V values over the 32 lanes.  Recursive halving: at each of log2(V)
 // steps a lane keeps the half of its values selected by one lane bit and adds its partner's copy of
 // that half.  Afterwards lane l holds a partial sum of value l >> (5 - log2 V), and the 32 / V
@@ -332,14 +349,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         // order (no bank conflicts for eight lanes 32 bytes apart); x is loaded in the same order.
         const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
         // The pair table is for the consumers alone: they write it while the producer already streams
-        // the first row blocks, and meet on a named barrier before the first lookup.  Entry e of the
-        // table (byte v = e / 32, lane column e % 32) is warp-uniform in v, so the constant reads
-        // do not diverge.
-        float2* ptab = reinterpret_cast<float2*>(smem);
-        for (int e = threadIdx.x; e < kPairTabBytes / 8; e += 32 * C) {
-            const int v = e >> 5;
-            ptab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
-        }
+        // the first row blocks, and meet on a named barrier before the first lookup.
+        build_pair_table(reinterpret_cast<float2*>(smem), threadIdx.x, 32 * C);
         pdl_wait();
         uint32_t xr[MT][WPL / 2];
 #pragma unroll
@@ -404,8 +415,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                     for (int wi = 0; wi < 4; wi++) {
 #pragma unroll
                         for (int p = 0; p < 4; p++) {
-                            // byte p of the word: table offset 256 * byte + 8 * lane in one permute
-                            const uint32_t off = prmt(words[wi], lcol, 0x6504u + 16u * p);
+                            const uint32_t off = pair_offset(words[wi], lcol, p);
                             const uint32_t wp = scale_pair(*reinterpret_cast<const float2*>(smem + off), scl[jj]);
 #pragma unroll
                             for (int tt = 0; tt < MT; tt++) fma_bf16x2(a0[tt], a1[tt], wp, xr[tt][4 * (4 * c + wi) + p]);

@@ -3,10 +3,13 @@
 //
 // The deep-fold README's execution-path table runs the N = 1 decode GEMV and the prefill GEMM of up
 // to 32 positions over packed weights, dequantizing only the current tile.  These shapes are bound
-// by the weight stream and by the integer work of the exact 16-entry lookups, so every
-// multiply-add goes to the tensor cores and the CUDA cores run the lookups alone:
+// by the weight stream and by the exact dequantization, so every multiply-add goes to the tensor
+// cores and the CUDA cores run the dequantization alone:
 //
 //   dequant warps:  packed codes (shared memory) -> exact bf16 w_hat -> tensor memory (tcgen05.st)
+//                   w_hat = bf16(fp32(T[c] * scale)) two weights at a time: the code byte indexes the
+//                   lane-replicated fp32 pair table {T[c0], T[c1]} in shared memory, one packed fp32x2
+//                   multiply by the scale, one bf16x2 conversion (see scale_pair)
 //   MMA warp:       tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
 //                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
 //
@@ -23,13 +26,6 @@
 // of accumulators, so that issuing costs the same on two warp schedulers; an issuer waits twice per
 // stage (x landed, A written) and commits once, converged, one elected lane issuing (elect_one).
 // The epilogue adds the four accumulators in a fixed order.
-//
-// Exponent folding.  A nonzero scale is 2^E * (1 + m/1024) with E = 2q + p, p in {0, 1}.  The table
-// row 1024 p + m holds 2^p * V[m][c] = bf16(T[c] * 2^p * (1 + m/1024)) exactly (rounding commutes
-// with powers of two), and 2^(2q) is added to every entry by adding q to its high byte (the
-// exponent's bits 7..1): four IMADs per group, no ALU work.  A zero scale reads the all-zero row.  A
-// negative scale (never produced by nf4_quantize, but allowed) flips the sign bits of the nonzero
-// entries on a warp-uniform branch.
 //
 // Warp roles, one helper per warp scheduler (warp w runs on scheduler w mod 4): warp 0 streams codes
 // (TMA), warps 1 and 3 issue the MMAs of even and odd stages (warp 1 also owns tensor memory), warp 2
@@ -63,10 +59,9 @@ struct NCfg {
     static constexpr int kU = 4;                                       // 64-k sub-stages per codes load stage
     static constexpr uint32_t kXSub = kJMax * 128;  // one 64-k x sub-tile (multiple of 1024 bytes)
     static constexpr uint32_t kXSlot = 2 * kXSub;
-    static constexpr uint32_t kVtabBytes = kVtabChunks * 16;
     static constexpr uint32_t kOffCodes = kAStages * kXSlot;
-    static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
-    static constexpr uint32_t kOffBars = kOffVtab + kVtabBytes;
+    static constexpr uint32_t kOffPtab = kOffCodes + kLoadStages * kLoadBytes;  // pair table
+    static constexpr uint32_t kOffBars = kOffPtab + kPairTabBytes;
     static constexpr uint32_t kBytes = kOffBars + 1024;
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(kDCols + 64 * kAStages <= 512, "tensor memory budget");
@@ -147,9 +142,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < kVtabChunks; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, &g_vtab[i]);
-    cp_async_commit();
-    cp_async_wait<0>();
+    build_pair_table(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -276,8 +269,8 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
         const int i = quarter * 32 + lane;        // MMA row
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint4* vt_lo = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
-        const uint4* vt_hi = vt_lo + kVtabHi;
+        const uint8_t* ptab = smem + C::kOffPtab;
+        const uint32_t lcol = static_cast<uint32_t>(lane) * 8;  // this lane's column of the pair table
         bool ok = true;
         // CTA-wide counts of the stages and codes load stages of the tiles before tile j: ring slots
         // and phases follow from them, so a set visits only its own stages.
@@ -348,37 +341,14 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                             const uint8_t* cb = crow + (u >> lbs) * bstride;
                             const uint32_t ch = static_cast<uint32_t>((((u & (BS - 1)) << ls) + sl) * 2);
                             const uint4 c0 = lds128(cb + 16 * (ch ^ swz)), c1 = lds128(cb + 16 * ((ch + 1) ^ swz));
-                            // scale = sign * 2^E * (1 + m/1024), E = e - 127 = 2q + p: table row
-                            // 1024 p + m, and q added to the high byte of every nonzero entry (code 7's
-                            // byte stays 0); a zero scale reads the zero row
-                            const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1]))));
-                            const uint32_t e = (sb >> 23) & 0xFFu;
-                            const uint32_t hq = (e + 1u) >> 1;                   // q + 64
-                            const uint32_t pbit = e + 1u - 2u * hq;
-                            const uint32_t row = e != 0u ? ((sb >> 13) & 0x3FFu) + (pbit << 10) : 2048u;
-                            const uint32_t qq = e != 0u ? hq - 64u : 0u;
-                            const uint4 tl = vt_lo[row];
-                            uint4 th = vt_hi[row];
-                            th.x += qq * 0x01010101u;
-                            th.y += qq * 0x00010101u;
-                            th.z += qq * 0x01010101u;
-                            th.w += qq * 0x01010101u;
-                            if (__any_sync(__activemask(), (sb >> 31) != 0u)) {  // a negative scale (rare)
-                                const uint32_t sg = ((sb >> 31) != 0u && e != 0u) ? 0x80808080u : 0u;
-                                th.x ^= sg;
-                                th.y ^= sg & 0x00FFFFFFu;
-                                th.z ^= sg;
-                                th.w ^= sg;
-                            }
+                            const float sc = __half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1])));
                             const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                             for (int w = 0; w < 8; w++) {
-                                uint32_t o4[4];
-                                lookup8(words[w], tl, th, P.m1, P.p16, o4);
-                                out[4 * w + 0] = o4[0];
-                                out[4 * w + 1] = o4[1];
-                                out[4 * w + 2] = o4[2];
-                                out[4 * w + 3] = o4[3];
+#pragma unroll
+                                for (int b = 0; b < 4; b++)
+                                    out[4 * w + b] = scale_pair(
+                                        *reinterpret_cast<const float2*>(ptab + pair_offset(words[w], lcol, b)), sc);
                             }
                         } else {
 #pragma unroll
