@@ -35,6 +35,7 @@ namespace {
 constexpr int kMaxWarps = 16;  // consumer warps per CTA (slices x row lanes)
 constexpr int kHalfWarps = 8;  // consumer warps of a CTA that leaves room for a second one
 constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
+constexpr int kMinStages = 3;          // ring stages a CTA with several K-slices keeps at least
 constexpr int kPairTabBytes = 256 * 32 * 8;  // code-byte table, one 8-byte column per lane (64 KB)
 
 // V table (the tensor-core kernels' dequantization, which writes bf16 operands rather than
@@ -449,8 +450,9 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     L.S = (G + GPW - 1) / GPW;
     // Launch shape (measured on the 3B-shaped decode pass: 144 launches in one graph, chained by
     // programmatic dependent launch):
-    //  - K over several slices: whole-SM CTAs, RMAX rows per warp, as many row lanes as the rows
-    //    need, the deepest ring that fits;
+    //  - K over several slices: whole-SM CTAs, RMAX rows per warp (fewer when a block that large
+    //    leaves a ring of fewer than kMinStages stages), as many row lanes as the rows need, the
+    //    deepest ring that fits;
     //  - one slice and up to 2 * kMaxWarps rows per SM: row blocks sized for about 1.7 blocks per
     //    CTA (two rows per warp when a block has at most 8 rows), so that the weights of a CTA's
     //    second block arrive while its first is computed, and a two-stage ring, which leaves room on
@@ -460,11 +462,17 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     bool half = false;
     bool cap_ring = false;    // ring no deeper than the CTA's row blocks
     int64_t slots = num_sms;  // CTAs resident at once
+    const int swin = ((2 * G + 15) / 16 + 1) * 16;
+    const auto stage_of = [&](int q, int r) {  // bytes of one ring stage (see the layout below)
+        return static_cast<int64_t>(q) * r * (K / 2 + swin + 16) + static_cast<int64_t>(L.S) * q * 32 * 4;
+    };
     if (L.S > 1) {
-        L.R = RMAX;
-        const int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
         const int qmax = L.S >= kMaxWarps ? 1 : kMaxWarps / L.S;
-        L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
+        for (L.R = RMAX;; L.R--) {
+            const int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
+            L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
+            if (L.R == 1 || (227 * 1024 - kPairTabBytes - 256) / stage_of(L.Q, L.R) >= kMinStages) break;
+        }
     } else if (N <= static_cast<int64_t>(2) * kMaxWarps * num_sms) {
         cap_ring = true;
         const int64_t rb = (N * 10 + 17LL * num_sms - 1) / (17LL * num_sms);  // rows per block
@@ -482,7 +490,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     const int64_t grid64 = nblocks_all < slots ? nblocks_all : slots;
     L.RB = L.Q * L.R;
     L.row_code_bytes = static_cast<int>(K / 2);
-    L.swin = ((2 * G + 15) / 16 + 1) * 16;
+    L.swin = swin;
     L.scales_off = L.RB * L.row_code_bytes;
     L.meta_off = L.scales_off + L.RB * L.swin;
     L.red_off = L.meta_off + 16 * L.RB;
