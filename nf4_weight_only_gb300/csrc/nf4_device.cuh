@@ -126,6 +126,13 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
+// Two floats from shared-window address `a` (8-byte aligned).
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+
 // Bulk (TMA-engine) copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) whose completion is counted as transaction bytes on mbarrier `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
         const int i = quarter * 32 + lane;        // MMA row
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint8_t* ptab = smem + C::kOffPtab;
+        const uint32_t ptab = sbase + C::kOffPtab;  // shared-window address of the pair table
         const uint32_t lcol = static_cast<uint32_t>(lane) * 8;  // this lane's column of the pair table
         bool ok = true;
         // CTA-wide counts of the stages and codes load stages of the tiles before tile j: ring slots
@@ -347,8 +347,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                             for (int w = 0; w < 8; w++) {
 #pragma unroll
                                 for (int b = 0; b < 4; b++)
-                                    out[4 * w + b] = scale_pair(
-                                        *reinterpret_cast<const float2*>(ptab + pair_offset(words[w], lcol, b)), sc);
+                                    out[4 * w + b] = scale_pair(lds_f2(ptab + pair_offset(words[w], lcol, b)), sc);
                             }
                         } else {
 #pragma unroll
