@@ -133,6 +133,13 @@ __device__ __forceinline__ float2 lds_f2(uint32_t a) {
     return v;
 }
 
+// 16 bits from shared-window address `a` (2-byte aligned).
+__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
 // Bulk (TMA-engine) copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) whose completion is counted as transaction bytes on mbarrier `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

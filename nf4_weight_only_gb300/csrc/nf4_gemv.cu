@@ -76,9 +76,6 @@ __global__ void build_vtab_kernel() {
     g_vtab[kVtabHi + row] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// Shared-memory copy of rows 0..1023 for the GEMM-form kernel: 1024 low-byte chunks,
-// then 1024 high-byte chunks (32 KB).  Chunk i of the copy.
-__device__ __forceinline__ const uint4* vtab_src32k(int i) { return &g_vtab[i < 1024 ? i : kVtabHi + (i - 1024)]; }
 
 // Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order, from a
 // V-table row held in registers (tensor-core kernels).
@@ -131,6 +128,22 @@ __device__ __forceinline__ void build_pair_table(float2* tab, int tid, int nthre
 // column offset is `lcol` (8 * lane): 256 * byte + lcol, built by one byte permute.
 __device__ __forceinline__ uint32_t pair_offset(uint32_t word, uint32_t lcol, int p) {
     return prmt(word, lcol, 0x6504u + 16u * static_cast<uint32_t>(p));
+}
+
+// The half-size pair table (kPairTab16Bytes, for kernels whose shared memory is short): 16 copies
+// side by side, slot e holding entry v = e / 16, and lane l reads copy l % 16.  A 64-bit load is
+// served per half-warp, so 16 copies keep every half-warp's lanes on distinct bank pairs.
+constexpr int kPairTab16Bytes = 256 * 16 * 8;
+__device__ __forceinline__ void build_pair_table16(float2* tab, int tid, int nthreads) {
+    for (int e = tid; e < kPairTab16Bytes / 8; e += nthreads) {
+        const int v = e >> 4;
+        tab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
+    }
+}
+// Offset of byte p's entry in the half-size table for a lane with lcol16 = 16 * (lane % 16):
+// 128 * byte + 8 * (lane % 16), a byte permute and a shift.
+__device__ __forceinline__ uint32_t pair_offset16(uint32_t word, uint32_t lcol16, int p) {
+    return prmt(word, lcol16, 0x6504u + 16u * static_cast<uint32_t>(p)) >> 1;
 }
 
 // First stage of summing each of V values over the 32 lanes.  Recursive halving: at each of log2(V)

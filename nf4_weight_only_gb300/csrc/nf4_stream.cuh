@@ -83,8 +83,8 @@ struct Cfg {
     static constexpr int kScaleStages = T == 256 ? 2 : 3;
     static constexpr uint32_t kXBytes = kJMax * 128;  // one x sub-tile (multiple of 1024)
     static constexpr uint32_t kOffCodes = kXStages * kXBytes;
-    static constexpr uint32_t kOffVtab = kOffCodes + kLoadStages * kLoadBytes;
-    static constexpr uint32_t kOffScales = kOffVtab + 32768;
+    static constexpr uint32_t kOffPtab = kOffCodes + kLoadStages * kLoadBytes;  // half-size pair table
+    static constexpr uint32_t kOffScales = kOffPtab + kPairTab16Bytes;
     static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
     static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
     static constexpr uint32_t kBytes = kOffBars + 1024;
@@ -320,9 +320,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < 2048; i += C::kThreads) cp_async16(smem + C::kOffVtab + 16 * i, vtab_src32k(i));
-    cp_async_commit();
-    cp_async_wait<0>();
+    build_pair_table16(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -494,7 +492,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
         const int i = quarter * 32 + lane;        // MMA row
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint4* vtab = reinterpret_cast<const uint4*>(smem + C::kOffVtab);
+        const uint32_t ptab = sbase + C::kOffPtab;                         // shared-window addresses
+        const uint32_t lcol16 = static_cast<uint32_t>(lane & 15) * 16;     // twice this lane's copy offset
         bool ok = true;
         int ep_uses = 0;
         // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
@@ -562,41 +561,14 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                         const uint8_t* crow = smem + C::kOffCodes + lslot * kLoadBytes + (u / BS) * kBoxStride + r * rowb;
                         const uint32_t ch = static_cast<uint32_t>(((u % BS) * t.s + sl) * 2);
                         const uint4 c0 = lds128(crow + 16 * (ch ^ swz)), c1 = lds128(crow + 16 * ((ch + 1) ^ swz));
-                        const uint16_t sc = *reinterpret_cast<const uint16_t*>(
-                            smem + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s);
-                        // scale = sign * 2^E * (1 + m/1024); w_hat = 2^E * V[m][c]: the table row
-                        // gives V, E is added to the exponent field of every entry.  An odd E flips
-                        // the exponent's low bit (bit 7 of the low byte) and carries into the high
-                        // byte; E >> 1 is added to the high byte (exponent >> 1), byte by byte.
-                        const uint32_t sb = __float_as_uint(__half2float(__ushort_as_half(sc)));
-                        const uint32_t m = (sb >> 13) & 0x3FFu;
-                        const int e = static_cast<int>((sb >> 23) & 0xFFu) - 127;
-                        const uint32_t pm = (e & 1) ? 0x80808080u : 0u;
-                        const uint32_t add = static_cast<uint32_t>(e >> 1) * 0x01010101u;
-                        const uint32_t sgn = (sb >> 31) ? 0x80808080u : 0u;
-                        uint4 tl = vtab[m];
-                        uint4 th = vtab[1024 + m];
-                        th.x = (th.x + add + ((tl.x & pm) >> 7)) ^ sgn;
-                        th.y = ((th.y + add + ((tl.y & pm) >> 7)) & 0x00FFFFFFu) ^ sgn;  // code 7 stays 0
-                        th.z = (th.z + add + ((tl.z & pm) >> 7)) ^ sgn;
-                        th.w = (th.w + add + ((tl.w & pm) >> 7)) ^ sgn;
-                        tl.x ^= pm;
-                        tl.y = (tl.y ^ pm) & 0x00FFFFFFu;
-                        tl.z ^= pm;
-                        tl.w ^= pm;
-                        if ((sb & 0x7FFFFFFFu) == 0u) {  // zero scale
-                            tl = make_uint4(0, 0, 0, 0);
-                            th = make_uint4(0, 0, 0, 0);
-                        }
+                        const float sc = __half2float(__ushort_as_half(
+                            lds_u16(sbase + C::kOffScales + sslot * kScaleSlot + soff + 2 * (kb & 7) * t.s)));
                         const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                         for (int w = 0; w < 8; w++) {
-                            uint32_t o4[4];
-                            lookup8(words[w], tl, th, P.m1, P.p16, o4);
-                            out[4 * w + 0] = o4[0];
-                            out[4 * w + 1] = o4[1];
-                            out[4 * w + 2] = o4[2];
-                            out[4 * w + 3] = o4[3];
+#pragma unroll
+                            for (int b = 0; b < 4; b++)
+                                out[4 * w + b] = scale_pair(lds_f2(ptab + pair_offset16(words[w], lcol16, b)), sc);
                         }
                     } else {
 #pragma unroll
