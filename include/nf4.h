@@ -30,9 +30,9 @@
  *     M, N and K must each be at most 2^31 - 1.
  *   - Non-finite inputs are outside the contract: results are unspecified, but no call faults.
  *   - The same inputs give the same output bytes on every call (no atomics, fixed reduction order).
- *   - The first linear call on a device builds a small constant table (one kernel and one wait on
- *     `stream`).  Make that first call outside stream capture: under capture it returns
- *     NF4_ERR_CAPTURE and touches neither the capture nor the stream.  Later calls may be captured.
+ *   - Every call may be captured into a CUDA graph (the kernels build their constant tables in
+ *     shared memory at launch; no call needs one-time device work), except the first call of
+ *     nf4_linear_host_noalloc on a device (see there).
  *   - Every pipeline wait inside the kernels is bounded (one second of wall-clock time per wait by
  *     default).  A wait that runs out records a code in the device error word, and the kernel
  *     drains and exits instead of hanging; the call itself has already returned NF4_OK and the
@@ -40,8 +40,7 @@
  *     nf4_check_device_error (the tests and the benchmark do after every timed region).
  *   - Every entry point except the ring calls (see their section) may be called from several host
  *     threads at once, on the same or different streams: the only shared state is the per-device
- *     capability cache (atomic), one-time kernel attributes (std::call_once) and the per-device
- *     constant table, built once under a mutex.
+ *     capability cache (atomic) and one-time kernel attributes (std::call_once).
  */
 #ifndef NF4_H
 #define NF4_H
@@ -67,8 +66,9 @@ typedef enum nf4_status {
     NF4_ERR_CUDA = 6,               /* a CUDA runtime call or kernel launch failed */
     NF4_ERR_MEMORY = 7,             /* memory of the wrong kind: a host pointer that is not page-locked,
                                        or a ring used on a device other than its own */
-    NF4_ERR_CAPTURE = 8             /* the first call on a device was made while `stream` is being captured
-                                       into a CUDA graph: its one-time set-up cannot run inside a capture */
+    NF4_ERR_CAPTURE = 8             /* the first nf4_linear_host_noalloc call on a device was made while
+                                       `stream` is being captured into a CUDA graph: its one-time set-up
+                                       cannot run inside a capture */
 } nf4_status;
 
 /*
@@ -230,8 +230,8 @@ nf4_status nf4_ring_destroy(nf4_ring* ring);
  * call rewrites every byte the kernels read, so nothing needs clearing).  Calls on one stream are
  * ordered and safe; calls whose work may overlap on the GPU (different streams with no ordering
  * between them) race on the array and give wrong results.
- * Set-up: the first call on a device looks up the array's device address (and, like the first
- * nf4_linear, builds the kernels' lookup table); make that first call before any stream capture.
+ * Set-up: the first call on a device looks up the array's device address; make that first call
+ * before any stream capture.
  * A first call made while `stream` is capturing returns NF4_ERR_CAPTURE and leaves the capture
  * untouched.
  */

@@ -66,11 +66,6 @@ nf4_status from_cuda(cudaError_t e) {
     return NF4_ERR_CUDA;
 }
 
-// ensure_tables reports a first call under stream capture as cudaErrorStreamCaptureUnsupported.
-nf4_status from_tables(cudaError_t e) {
-    return e == cudaErrorStreamCaptureUnsupported ? NF4_ERR_CAPTURE : from_cuda(e);
-}
-
 }  // namespace
 
 namespace nf4 {
@@ -93,7 +88,7 @@ const char* nf4_status_str(nf4_status status) {
         case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA call or launch failed";
         case NF4_ERR_MEMORY: return "NF4_ERR_MEMORY: host memory not page-locked, or a ring used on another device";
         case NF4_ERR_CAPTURE:
-            return "NF4_ERR_CAPTURE: first call on this device made under stream capture (make one call outside capture first)";
+            return "NF4_ERR_CAPTURE: first nf4_linear_host_noalloc call on this device made under stream capture (make one call outside capture first)";
     }
     return "NF4 status: unknown code";
 }
@@ -138,7 +133,6 @@ nf4_status nf4_linear_grouped(const uint16_t* x, int64_t M, int64_t K, int count
     }
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
-    if ((st = from_tables(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
     // drop empty problems, keep the order
     const uint8_t* c[nf4::kMaxGroupedLinears];
     const uint16_t* sc[nf4::kMaxGroupedLinears];
@@ -246,7 +240,6 @@ nf4_status nf4_linear(const uint16_t* x, const uint8_t* codes, const uint16_t* s
     if (overlap(y, yb, x, xb) || overlap(y, yb, codes, cb) || overlap(y, yb, scales, sb)) return NF4_ERR_ALIAS;
     int dev = 0, sms = 0;
     if ((st = current_device(&dev, &sms)) != NF4_OK) return st;
-    if ((st = from_tables(nf4::ensure_tables(dev, stream))) != NF4_OK) return st;
     if (M <= nf4::kGemvMaxTokens && K <= nf4::gemv_max_k(M))
         return from_cuda(nf4::launch_gemv(x, codes, scales, y, M, N, K, sms, stream));
     return from_cuda(nf4::launch_stream(x, 1, &codes, &scales, &y, &N, M, K, sms, stream));

@@ -42,13 +42,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// Per-bit select: bits of `b` where `mask` is 1, bits of `a` where it is 0.
-__device__ __forceinline__ uint32_t select_bits(uint32_t a, uint32_t b, uint32_t mask) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xD8;" : "=r"(d) : "r"(a), "r"(b), "r"(mask));
-    return d;
-}
-
 // acc + lo16(w) * lo16(x) and acc + hi16(w) * hi16(x) with bf16 operands: the product of two bf16
 // numbers is exact in fp32, so each step rounds once (fp32 accumulate).
 __device__ __forceinline__ void fma_bf16x2(float& acc_lo, float& acc_hi, uint32_t w, uint32_t x) {
@@ -81,25 +74,6 @@ __device__ __forceinline__ uint16_t ld_nc_u16(const uint16_t* p) {
     uint16_t v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
-}
-
-// Integer work steered onto the FMA pipe (IMAD) instead of the half-rate ALU pipe.  ptxas turns a
-// multiply by a compile-time constant into a shift or logic op, so the multipliers arrive as
-// kernel arguments whose values it cannot see: m1 = 0xFFFFFFFF, p16 = 0x10000.
-__device__ __forceinline__ uint32_t not_fma(uint32_t w, uint32_t m1) {  // w * -1 + -1 = ~w
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, %2, %2;" : "=r"(d) : "r"(w), "r"(m1));
-    return d;
-}
-__device__ __forceinline__ uint32_t shr16_fma(uint32_t w, uint32_t p16) {  // hi32(w * 2^16) = w >> 16
-    uint32_t d;
-    asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(p16));
-    return d;
-}
-__device__ __forceinline__ uint32_t shl4_fma(uint32_t w) {  // w << 4 (ptxas keeps constant left shifts on IMAD)
-    uint32_t d;
-    asm("mul.lo.u32 %0, %1, 16;" : "=r"(d) : "r"(w));
-    return d;
 }
 
 // 16-byte asynchronous global -> shared copy; bytes past `src_bytes` (0..16) are zero-filled.

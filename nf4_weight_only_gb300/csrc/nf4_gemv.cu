@@ -38,65 +38,6 @@ constexpr int kHalfSmem = 113 * 1024;  // shared memory of such a CTA
 constexpr int kMinStages = 3;          // ring stages a CTA with several K-slices keeps at least
 constexpr int kPairTabBytes = 256 * 32 * 8;  // code-byte table, one 8-byte column per lane (64 KB)
 
-// V table (the tensor-core kernels' dequantization, which writes bf16 operands rather than
-// multiply-adds).  Scale factorisation: a nonzero fp16 scale is 2^E * (1 + m/1024) with m its top ten
-// fraction bits (fp16 subnormals included, read as binary32).  Rounding commutes with multiplication
-// by a power of two, so w_hat = bf16(fp32(T[c] * scale)) = 2^E * V[m][c] with V[m][c] =
-// bf16(fp32(T[c] * (1 + m/1024))).  Per (row, group) a lane holds its V row as eight registers (low
-// and high byte planes, codes 0-7 and 8-15), and `prmt` looks up one byte plane for four codes.
-// Row R holds the 16 bf16 entries of one scale class as two 16-byte chunks: the low bytes
-// {L(0..3), L(4..7), L(15..12), L(11..8)} at chunk R and the high bytes in the same order at chunk
-// kVtabHi + R, L / H being the low / high byte of the entry for code c.  Codes 8..15 are stored in
-// reverse so that the complemented nibble 15 - c (one IMAD) indexes them directly.
-// Rows 0..1023 hold V[m][c]; rows 1024..2047 hold 2 * V[m][c] (the same values one binade up,
-// exact); row 2048 is all zeros.  The GEMM-form streaming kernel reads rows 0..1023; the small-M
-// streaming kernel reads all of them.
-constexpr int kVtabRows = 2049;
-constexpr int kVtabHi = 2056;                  // first high-byte chunk
-constexpr int kVtabChunks = kVtabHi + 2056;    // 4112 chunks (65,792 bytes)
-__device__ uint4 g_vtab[kVtabChunks];
-
-__global__ void build_vtab_kernel() {
-    const int row = blockIdx.x * blockDim.x + threadIdx.x;
-    if (row >= kVtabRows) return;
-    const int m = row & 1023;  // mantissa class of the scale
-    const float s1 = __uint_as_float(0x3F800000u | (static_cast<uint32_t>(m) << 13));  // 1 + m/1024
-    uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
-    if (row < 2048) {
-#pragma unroll
-        for (int c = 0; c < 16; c++) {
-            uint32_t b = bf16_bits(__fmul_rn(kNF4[c], s1));
-            if (row >= 1024) b = bf16_bits(2.0f * __uint_as_float(b << 16));  // exact: one binade up
-            const int slot = c < 8 ? c : 8 + (15 - c);  // byte position inside the 16-byte plane
-            lo[slot >> 2] |= (b & 0xFFu) << (8 * (slot & 3));
-            hi[slot >> 2] |= (b >> 8) << (8 * (slot & 3));
-        }
-    }
-    g_vtab[row] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    g_vtab[kVtabHi + row] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-}
-
-
-// Eight codes (weight 2i in the low nibble of byte i) -> four bf16 pairs, weights in order, from a
-// V-table row held in registers (tensor-core kernels).
-// 18 ALU-pipe instructions (PRMT / LOP3) and 4 FMA-pipe ones (selector preparation).
-__device__ __forceinline__ void lookup8(uint32_t w, const uint4& tl, const uint4& th, uint32_t m1, uint32_t p16,
-                                        uint32_t out[4]) {
-    const uint32_t nw = not_fma(w, m1);  // nibble 15 - c: codes 8..15 index the reversed second half
-    const uint32_t w4 = shl4_fma(w);
-    const uint32_t wh = shr16_fma(w, p16), nwh = shr16_fma(nw, p16);
-    uint32_t msk = prmt(w4, w, 0xD9C8u);  // byte i = 0xFF iff code i >= 8 (i = 0..3)
-    uint32_t lo = select_bits(prmt(tl.x, tl.y, w), prmt(tl.z, tl.w, nw), msk);
-    uint32_t hi = select_bits(prmt(th.x, th.y, w), prmt(th.z, th.w, nw), msk);
-    out[0] = prmt(lo, hi, 0x5140u);
-    out[1] = prmt(lo, hi, 0x7362u);
-    msk = prmt(w4, w, 0xFBEAu);  // codes 4..7
-    lo = select_bits(prmt(tl.x, tl.y, wh), prmt(tl.z, tl.w, nwh), msk);
-    hi = select_bits(prmt(th.x, th.y, wh), prmt(th.z, th.w, nwh), msk);
-    out[2] = prmt(lo, hi, 0x5140u);
-    out[3] = prmt(lo, hi, 0x7362u);
-}
-
 // Two dequantized weights from one code byte: the pair-table entry {T[c0], T[c1]} (fetched by the
 // caller) times the scale in one packed fp32 multiply, then both rounded to bf16 (c0 in the low
 // half).  Equals bf16(fp32(T[c] * scale)) for each code.
@@ -448,12 +389,6 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     }
 }
 
-struct TableState {
-    std::mutex mu;
-    bool ready[64] = {};
-};
-TableState g_tables;
-
 template <int MT, int LPG, int RMAX>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
     constexpr int GPW = 32 / LPG;
@@ -713,8 +648,6 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
         P.M = static_cast<int>(M);
         P.K = static_cast<int>(K);
         P.G = static_cast<int>(K / kGroup);
-        P.m1 = 0xFFFFFFFFu;
-        P.p16 = 0x10000u;
         if (M <= 64) return launch_stream_t<64>(x, P, M, K, stream);
         if (M <= 128) return launch_stream_t<128>(x, P, M, K, stream);
         return launch_stream_t<256>(x, P, M, K, stream);
@@ -748,8 +681,6 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
     P.M = static_cast<int>(M);
     P.K = static_cast<int>(K);
     P.G = static_cast<int>(G);
-    P.m1 = 0xFFFFFFFFu;
-    P.p16 = 0x10000u;
     // K-slices of a partial tile: as many as fit 128 MMA rows, the B tile's pseudo-token columns and G.
     P.r_rem = static_cast<int>(rpc % 128);
     // (a power of two, so that a row's slices are consecutive lanes of one warp)
@@ -822,27 +753,6 @@ cudaError_t read_and_clear_error(int* code) {
 // Largest K the register-resident layout covers: kMaxWarps slices of 32 (one lane per group) or 16
 // groups (two lanes per group).
 int64_t gemv_max_k(int64_t M) { return static_cast<int64_t>(kMaxWarps) * (M == 1 ? 32 : 16) * kGroup; }
-
-cudaError_t ensure_tables(int device, cudaStream_t stream) {
-    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_tables.mu);
-    if (g_tables.ready[device]) return cudaSuccess;
-    // The build waits for `stream`, which a capture forbids: refuse before touching it.
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-        cudaGetLastError();
-        return cudaErrorStreamCaptureUnsupported;
-    }
-    if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
-    build_vtab_kernel<<<(kVtabRows + 255) / 256, 256, 0, stream>>>();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // One-time wait so that later calls on any stream see the table.
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return e;
-    g_tables.ready[device] = true;
-    return cudaSuccess;
-}
 
 cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* const* codes,
                                 const uint16_t* const* scales, uint16_t* const* ys, const int64_t* Ns, int64_t M,

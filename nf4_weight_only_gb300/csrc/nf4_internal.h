@@ -40,11 +40,6 @@ cudaError_t launch_embed(const int32_t* ids, int64_t n_ids, const uint8_t* codes
                          int64_t K, uint16_t* out, int num_sms, cudaStream_t stream);
 cudaError_t read_and_clear_embed_error(int* code);
 
-// Per-device constant table used by the linear kernels (built once per device with one wait on
-// `stream`).  Returns cudaErrorStreamCaptureUnsupported, touching nothing, when the table is not
-// built yet and `stream` is being captured.
-cudaError_t ensure_tables(int device, cudaStream_t stream);
-
 // The C-ABI layer's device check (an nf4_status value): the current device and its SM count.
 int abi_current_device(int* device, int* sms);
 // Records a CUDA error for nf4_last_cuda_error (no-op for cudaSuccess).

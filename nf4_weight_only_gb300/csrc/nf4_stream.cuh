@@ -1,46 +1,29 @@
-// NF4 weight streaming for small M (decode and prefill up to 32 positions) on the tcgen05 tensor
-// cores, sm_103a.
-//
-// y[M, N] = x[M, K] * w_hat[N, K]^T for 1 <= M <= 32 (deep-fold README, execution-path table: the
-// N=1 decode GEMV and the prefill GEMM of up to 32 positions, both dequantizing only the current
-// tile of the packed weights).  These shapes are bound by the weight stream and by the integer work
-// of the 16-entry lookups, not by multiply-add throughput, so this kernel moves every multiply-add
-// onto the tensor cores and leaves the CUDA cores the lookups alone:
+// NF4 GEMM-form weight streaming for prefill (M >= 33 positions) on the tcgen05 tensor cores,
+// sm_103a: y[M, N] = x[M, K] * w_hat[N, K]^T, dequantizing only the current tile of the packed
+// weights (deep-fold README, execution-path table: the prefill GEMM over packed weights).
+// stream_kernel<T> is instantiated for T = 64, 128 and 256 tokens per CTA ("wide" tiles); M <= 32
+// runs the small-M kernel of nf4_narrow.cuh, M <= 3 with K in range the CUDA-core GEMV.
 //
 //   dequant warps:  packed codes (shared memory) -> exact bf16 w_hat -> tensor memory (tcgen05.st)
-//   one thread:     tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
-//                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
+//                   w_hat = bf16(fp32(T[c] * scale)) two weights at a time from the half-size fp32
+//                   pair table in shared memory (pair_offset16, scale_pair in nf4_gemv.cu)
+//   one warp:       tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
+//                   (TMA, 128-byte swizzle), D = fp32 accumulator in tensor memory (N = T)
 //
-// K-slices.  A CTA owns a contiguous range of output rows, processed as tiles of R rows.  The 128
-// MMA rows of a tile are R rows x S K-slices (R * S <= 128): MMA row i = r * S + s holds row r's
-// groups s, S + s, 2S + s, ...; stage kb covers groups kb*S .. kb*S + S - 1, which are contiguous in
-// memory for every row.  The B tile holds, for each token t and slice s, the 64 x values of group
-// kb*S + s as pseudo-token column j = t * S + s, so D[r*S + s][t*S + s] is row r's partial sum over
-// slice s; the epilogue adds the S partials of each (row, token) in slice order.  The off-diagonal
-// columns are computed and dropped (the tensor cores have the throughput to spare).  This lets a
-// CTA with only a dozen rows still fill all 128 MMA rows and all 128 dequant lanes, so the grid is
-// one CTA per SM with a balanced row range each, for any N.
-//
-// Rings.  Codes move in load stages of U 64-k sub-stages (U = 4 for S = 1, else 2; one TMA box of
-// all rows x U*S groups, 128 bytes a row where possible: the TMA engine moves short rows slowly;
-// two boxes of 32*S-byte rows for S >= 3); x moves per sub-stage (one box of T tokens x S groups);
-// scales per 8 sub-stages (zero-filling 16-byte copies of each row's window).  The codes and scale
-// rings are released by the dequant sets whose stages read them, the x ring by the MMAs, and the
+// A CTA owns one tile of 128 rows x T tokens (grid: row tiles x token tiles).  Codes move in load
+// stages of four 64-k sub-stages (one TMA box of 128 rows x 128 bytes), x per 64-k sub-tile (one box
+// of T tokens), scales per 8 sub-stages (zero-filling 16-byte copies of each row's window).  The
+// codes and scale rings are released by the dequant sets whose stages read them, the x ring and the
 // tensor-memory ring of A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
 //
 // Warp roles: warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp copies
-// scales), warp 1 owns tensor memory and one lane issues the MMAs, warps 2 .. 4*kSets+1 are kSets
-// sets of four dequant warps (a set takes every kSets-th stage and waits only for the codes and
-// scales of its own stages; the four warps of a set cover the four 32-lane quarters of tensor
-// memory) that also run the epilogue of every kSets-th tile, and the last warp streams x.
-// kSets = 4 for the wide tiles (608 threads) and 3 for T <= 32 (480 threads): with fewer sets the
-// lookups' dependent integer chains leave the dequant warps latency-bound.
-// Weights do not depend on the previous kernel in the stream, so warp 0 never waits for it; only x
-// and y do.  Each producer runs as far ahead as its own ring allows.
-//
-// The per-device V table (32 KB, see nf4_gemv.cu) gives V[m][c] = bf16(T[c] * (1 + m/1024)); the
-// scale's exponent is added in registers (an odd exponent flips the exponent's low bit in the low
-// byte and carries into the high byte; the rest is added to the high byte).
+// scales), warp 1 owns tensor memory and issues the MMAs (converged, one elected lane), warps
+// 2 .. 4*kSets+1 are kSets = 4 sets of four dequant warps (a set takes every fourth stage and waits
+// only for the codes and scales of its own stages; the four warps of a set cover the four 32-lane
+// quarters of tensor memory), which also run the epilogue, and the last warp streams x.  Weights do
+// not depend on the previous kernel in the stream, so warp 0 never waits for it; only x and y do.
+// (The configuration and tile arithmetic below still carry the K-slice fields of the shared tile
+// description, which the wide tiles fix at one slice.)
 // Every mbarrier wait is bounded; a wait that runs out records an error code, drains the copies and
 // MMAs in flight (bounded again) and frees tensor memory.
 #pragma once
@@ -113,7 +96,6 @@ struct Params {
     int r_rem;                      // rows of a CTA's partial tile (rstar % 128; 0 = none)
     int s_rem;                      // its K-slices (r_rem * s_rem <= 128)
     int M, K, G;
-    uint32_t m1, p16;               // 0xFFFFFFFF and 0x10000 (multipliers of the lookup, see lookup8)
 };
 
 // Codes of each problem, uint8 [N][K/2]: full tiles load boxes of 128 rows x 128 bytes (4 groups,
@@ -254,6 +236,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     stream_kernel(const __grid_constant__ CUtensorMap x_full, const __grid_constant__ CUtensorMap x_rem,
                   const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
     using C = Cfg<T>;
+    static_assert(C::kWide, "stream_kernel runs the wide tiles only (T >= 64)");
     constexpr int NA = C::kAStages, NX = C::kXStages, NL = C::kLoadStages, NSS = C::kScaleStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -308,6 +308,47 @@ def test_outputs_identical_across_fresh_processes(nf4):
     assert len(set(hashes)) == 1, hashes
 
 
+_FIRST_CALL_CAPTURED_SCRIPT = r"""
+import torch
+import nf4_weight_only_gb300 as nf4
+from nf4_weight_only_gb300 import synth
+nf4.load()
+dev = torch.device("cuda", 0)
+cases = []
+for m, n, k, seed in [(1, 1000, 5120, 0), (8, 640, 2048, 1), (300, 384, 1024, 2)]:
+    codes, scales = synth.device_packed(830 + seed, n, k, dev)  # torch only: no library call yet
+    x = synth.device_activations_bf16(840 + seed, m, k, dev)
+    cases.append((x, codes, scales, torch.empty((m, n), dtype=torch.bfloat16, device=dev)))
+torch.cuda.synchronize()
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):  # the process's first library calls, captured
+    for x, codes, scales, y in cases:
+        nf4.nf4_linear(x, codes, scales, y, stream=s)
+g.replay()
+torch.cuda.synchronize()
+for x, codes, scales, y in cases:
+    ref = torch.empty_like(y)
+    nf4.nf4_linear(x, codes, scales, ref)
+    torch.cuda.synchronize()
+    assert torch.equal(ref.view(torch.int16), y.view(torch.int16))
+print("OK", nf4.nf4_check_device_error())
+"""
+
+
+def test_first_calls_may_be_captured(nf4):
+    """In a fresh process the first library calls (GEMV, small-M and GEMM-form kernels) are made
+    inside a CUDA graph capture: the replayed graph gives the same bytes as eager calls afterwards
+    (no call needs one-time device work outside a capture)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_CAPTURED_SCRIPT], cwd=root, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "OK 0" in r.stdout, r.stdout[-500:]
+
+
 def test_first_call_of_a_fresh_host_thread(nf4, o):
     """A host thread whose first CUDA work is a library call on the tensor-core paths (M = 8 and
     M = 300; their launch encodes tensor maps through the driver, which needs a current context)

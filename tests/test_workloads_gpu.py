@@ -116,7 +116,7 @@ def test_decode_3b_pass_graph(nf4, o):
     stream = torch.cuda.Stream(device=DEV)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        _run_pass(nf4, layers, xs, ys, stream)  # the first call per device builds its table
+        _run_pass(nf4, layers, xs, ys, stream)  # warm-up (kernel attributes, tensor maps) before the capture
     torch.cuda.synchronize()
     ys = _empty_outputs(layers, 1)
     graph = torch.cuda.CUDAGraph()
