@@ -114,6 +114,64 @@ __device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
     return v;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Dequantization by pair table: w_hat = bf16(fp32(T[c] * scale)), two weights at a time.  A code
+// byte (two codes, low nibble first) indexes a 256-entry shared-memory table whose entry is the
+// fp32 pair {T[low nibble], T[high nibble]}; one packed fp32x2 multiply by the group's scale (round
+// to nearest) and one bf16x2 conversion (round to nearest even) give both weights.  The table is
+// replicated so that a warp's 64-bit loads never conflict, whatever the codes are.
+// ---------------------------------------------------------------------------------------------
+constexpr int kPairTabBytes = 256 * 32 * 8;  // 32 copies, one 8-byte column per lane (64 KB)
+
+// Two dequantized weights from one code byte: the pair-table entry {T[c0], T[c1]} (fetched by the
+// caller) times the scale in one packed fp32 multiply, then both rounded to bf16 (c0 in the low
+// half).  Equals bf16(fp32(T[c] * scale)) for each code.
+__device__ __forceinline__ uint32_t scale_pair(float2 t, float s) {
+    uint32_t d;
+    asm("{\n\t.reg .b64 t, s2, r;\n\t.reg .f32 p0, p1;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "mov.b64 s2, {%3, %3};\n\t"
+        "mul.rn.f32x2 r, t, s2;\n\t"
+        "mov.b64 {p0, p1}, r;\n\t"
+        "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+        : "=r"(d)
+        : "f"(t.x), "f"(t.y), "f"(s));
+    return d;
+}
+
+// Writes the pair table (kPairTabBytes at `tab`): slot e holds entry v = e / 32, the fp32 pair
+// {T[v & 15], T[v >> 4]} of code byte v, for lane column e % 32.  Threads `tid` of `nthreads` (a
+// multiple of 32) share the work; a warp's 32 slots belong to one entry, so the constant reads do
+// not diverge.
+__device__ __forceinline__ void build_pair_table(float2* tab, int tid, int nthreads) {
+    for (int e = tid; e < kPairTabBytes / 8; e += nthreads) {
+        const int v = e >> 5;
+        tab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
+    }
+}
+
+// Shared-memory offset of the pair-table entry of byte p (0..3) of a code word for the lane whose
+// column offset is `lcol` (8 * lane): 256 * byte + lcol, built by one byte permute.
+__device__ __forceinline__ uint32_t pair_offset(uint32_t word, uint32_t lcol, int p) {
+    return prmt(word, lcol, 0x6504u + 16u * static_cast<uint32_t>(p));
+}
+
+// The half-size pair table (kPairTab16Bytes, for kernels whose shared memory is short): 16 copies
+// side by side, slot e holding entry v = e / 16, and lane l reads copy l % 16.  A 64-bit load is
+// served per half-warp, so 16 copies keep every half-warp's lanes on distinct bank pairs.
+constexpr int kPairTab16Bytes = 256 * 16 * 8;
+__device__ __forceinline__ void build_pair_table16(float2* tab, int tid, int nthreads) {
+    for (int e = tid; e < kPairTab16Bytes / 8; e += nthreads) {
+        const int v = e >> 4;
+        tab[e] = make_float2(kNF4[v & 15], kNF4[v >> 4]);
+    }
+}
+// Offset of byte p's entry in the half-size table for a lane with lcol16 = 16 * (lane % 16):
+// 128 * byte + 8 * (lane % 16), a byte permute and a shift.
+__device__ __forceinline__ uint32_t pair_offset16(uint32_t word, uint32_t lcol16, int p) {
+    return prmt(word, lcol16, 0x6504u + 16u * static_cast<uint32_t>(p)) >> 1;
+}
+
 // Bulk (TMA-engine) copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) whose completion is counted as transaction bytes on mbarrier `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -98,45 +98,45 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
     }
 }
 
-// Each thread expands 8 code bytes (16 weights, a quarter group) into 32 bytes of bf16, for
-// kDequantQuarters quarters per step whose loads it issues first.
-constexpr int kDequantQuarters = 4;
-
-__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ codes,
-                                                      const uint16_t* __restrict__ scales, int64_t groups,
-                                                      uint16_t* __restrict__ w_hat) {
-    __shared__ float table[16];
-    if (threadIdx.x < 16) table[threadIdx.x] = kNF4[threadIdx.x];
-    __syncthreads();
-    const int64_t quarters = groups * 4;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // step i of a thread covers quarters q0 + u * stride, u < kDequantQuarters (coalesced per u)
-    for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q0 < quarters;
-         q0 += stride * kDequantQuarters) {
-        uint2 cw[kDequantQuarters];
-        uint16_t sc[kDequantQuarters];
+// Eight weights (four code bytes, one 32-bit word) -> four bf16 pairs through the half-size pair
+// table at shared-window address `ptab` (lcol16 = 16 * (lane % 16)).
+__device__ __forceinline__ void dequant8(uint32_t word, float s, uint32_t ptab, uint32_t lcol16, uint32_t (&out)[4]) {
 #pragma unroll
-        for (int u = 0; u < kDequantQuarters; u++) {
-            const int64_t q = q0 + u * stride;
-            cw[u] = q < quarters ? __ldcs(reinterpret_cast<const uint2*>(codes) + q) : make_uint2(0, 0);
-            sc[u] = q < quarters ? scales[q >> 2] : static_cast<uint16_t>(0);
+    for (int b = 0; b < 4; b++) out[b] = scale_pair(lds_f2(ptab + pair_offset16(word, lcol16, b)), s);
+}
+
+// Dequant: 8-weight chunks (chunk c = weights 8c .. 8c+7 of the flat [N][K] array, group c / 8).  In
+// each of kDequantUnroll rounds lane l of a warp takes chunk base + 32 * round + l, so one warp's
+// 16-byte stores cover 512 contiguous bytes of w_hat; all rounds' loads are issued first.
+constexpr int kDequantUnroll = 4;
+constexpr int kDequantThreads = 512;
+
+__global__ void __launch_bounds__(kDequantThreads, 2048 / kDequantThreads) dequant_kernel(const uint32_t* __restrict__ codes,
+                                                                  const uint16_t* __restrict__ scales, int64_t chunks,
+                                                                  uint16_t* __restrict__ w_hat) {
+    __shared__ __align__(16) float2 tab[kPairTab16Bytes / 8];
+    build_pair_table16(tab, threadIdx.x, blockDim.x);
+    __syncthreads();
+    const uint32_t ptab = smem_u32(tab);
+    const int lane = threadIdx.x & 31;
+    const uint32_t lcol16 = static_cast<uint32_t>(lane & 15) * 16;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t c0 = warp * 32 * kDequantUnroll; c0 < chunks; c0 += warps * 32 * kDequantUnroll) {
+        uint32_t cw[kDequantUnroll];
+        uint16_t sc[kDequantUnroll];
+#pragma unroll
+        for (int u = 0; u < kDequantUnroll; u++) {
+            const int64_t c = c0 + 32 * u + lane;
+            cw[u] = c < chunks ? __ldcs(codes + c) : 0u;
+            sc[u] = c < chunks ? scales[c >> 3] : static_cast<uint16_t>(0);
         }
 #pragma unroll
-        for (int u = 0; u < kDequantQuarters; u++) {
-            const int64_t q = q0 + u * stride;
-            if (q >= quarters) break;
-            const float s = __half2float(__ushort_as_half(sc[u]));
-            uint32_t out[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t byte = ((j < 4 ? cw[u].x : cw[u].y) >> (8 * (j & 3))) & 0xFFu;
-                const uint32_t lo = bf16_bits(__fmul_rn(table[byte & 0xFu], s));
-                const uint32_t hi = bf16_bits(__fmul_rn(table[byte >> 4], s));
-                out[j] = lo | (hi << 16);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(w_hat + q * 16);
-            __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
-            __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
+        for (int u = 0; u < kDequantUnroll; u++) {
+            const int64_t c = c0 + 32 * u + lane;
+            uint32_t out[4];
+            dequant8(cw[u], __half2float(__ushort_as_half(sc[u])), ptab, lcol16, out);
+            if (c < chunks) __stcs(reinterpret_cast<uint4*>(w_hat) + c, make_uint4(out[0], out[1], out[2], out[3]));
         }
     }
 }
@@ -145,7 +145,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
 __device__ int g_embed_error;
 
 // Packed embedding rows: thread per quarter group (16 weights) of a requested row, the same exact
-// arithmetic as dequant_kernel; an id outside [0, V) writes zeros and records 41.
+// arithmetic as dequant_kernel (bf16(fp32(T[c] * scale)) per weight, from a 16-entry table: a
+// launch of a few thousand rows is too short to amortise the pair table); an id outside [0, V)
+// writes zeros and records 41.
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids, int64_t n_ids,
                                                     const uint8_t* __restrict__ codes,
                                                     const uint16_t* __restrict__ scales, int64_t V, int64_t K,
@@ -201,10 +203,12 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes
 
 cudaError_t launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t N, int64_t K,
                            uint16_t* w_hat, int num_sms, cudaStream_t stream) {
-    const int64_t groups = N * (K / kGroup);
-    if (groups == 0) return cudaSuccess;
-    const int grid = grid_for(256 * kDequantQuarters, groups * 4, num_sms, 8);
-    dequant_kernel<<<grid, 256, 0, stream>>>(codes, scales, groups, w_hat);
+    const int64_t chunks = N * K / 8;
+    if (chunks == 0) return cudaSuccess;
+    const int grid = grid_for(static_cast<int64_t>(kDequantThreads) * kDequantUnroll, chunks, num_sms,
+                              2048 / kDequantThreads);
+    dequant_kernel<<<grid, kDequantThreads, 0, stream>>>(reinterpret_cast<const uint32_t*>(codes), scales, chunks,
+                                                          w_hat);
     return cudaGetLastError();
 }
 
