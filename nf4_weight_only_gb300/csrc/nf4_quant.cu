@@ -49,50 +49,90 @@ __device__ __forceinline__ uint32_t code_of(float r, const float* thr) {
     return c;
 }
 
-// A warp takes kQuantGroups consecutive groups per step and issues all their loads before it
-// computes any of them (one 256-byte load per group would leave too few bytes in flight for HBM).
-// Within a group, lane l holds weights 2l and 2l+1 and writes code byte l.  The groups' steps carry
-// no branches, so their reductions, divisions and searches interleave: an all-zero group divides by
-// 1 instead of by s = 0, which turns its weights (+0 or -0) into r = +-0, whose code is 7 (T[7] = 0)
-// as the format requires.
-constexpr int kQuantGroups = 8;
+// Code of w / d with r = RN(w / d) as the format defines it, cheaply in almost every case.  Fast
+// path: q = w * rcp, rcp an approximation of 1 / d (relative error <= 2^-23), so |q - r| <= 2^-22 |r|;
+// a bucket table indexed by round(32 q + 32) gives the code c0 at the bucket's low end and the one
+// threshold inside the bucket (buckets are 1/32 wide, thresholds at least 0.08 apart), so the
+// candidate code is c0 + (q >= threshold).  The candidate is accepted only when q lies strictly inside
+// that code's interval shrunk by 2^-20 of each bound's magnitude (bnd): then r, within 2^-22 |r| of
+// q, lies inside the interval as well and has the same code.  Otherwise (a weight within about a
+// millionth of a threshold, or a non-finite q from a subnormal divisor) the exact division and search
+// decide.  The result never depends on the fast path: only its speed does.
+__device__ __forceinline__ uint32_t fast_code(float w, float rcp, float d, const float* thr, const float2* bnd,
+                                              const float2* bkt) {
+    const float q = __fmul_rn(w, rcp);
+    // 2^23 + 32 + 32 q rounded to an integer: its low bits are the bucket (0..64 for |q| <= 1)
+    const uint32_t j = min(static_cast<uint32_t>(__float_as_int(__fmaf_rn(q, 32.0f, 8388640.0f)) - 0x4B000000), 64u);
+    const float2 b = bkt[j];
+    uint32_t c = __float_as_uint(b.x) + (q >= b.y ? 1u : 0u);
+    const float2 lh = bnd[c];
+    if (!(q > lh.x && q < lh.y)) c = code_of(__fdiv_rn(w, d), thr);
+    return c;
+}
 
-__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ w, int64_t groups,
-                                                       uint8_t* __restrict__ codes,
+// Eight lanes per group, eight weights per lane: a warp takes kQuantGroups consecutive groups per
+// step, as kQuantGroups / 4 rounds of four groups (lane l: group 4 * round + l / 8 of the step,
+// weights 8 (l % 8) .. 8 (l % 8) + 7 of it), and issues every round's loads before it computes any.
+// A group's absmax takes three shuffle steps; a lane packs its eight codes into one 32-bit word, so
+// a round's code stores are 128 contiguous bytes.  An all-zero group divides by 1 instead of by s = 0,
+// which turns its weights (+0 or -0) into r = +-0, whose code is 7 (T[7] = 0) as the format requires.
+constexpr int kQuantGroups = 8;
+constexpr int kQuantRounds = kQuantGroups / 4;
+
+__global__ void __launch_bounds__(256, 5) quantize_kernel(const float* __restrict__ w, int64_t groups,
+                                                       uint32_t* __restrict__ codes,
                                                        uint16_t* __restrict__ scales) {
     __shared__ float thr[16];
+    __shared__ float2 bnd[16];  // per code: its interval [thr[c-1], thr[c]) shrunk by 2^-20 of each bound
+    __shared__ float2 bkt[65];  // per bucket: (code at its low end as integer bits, threshold inside or +inf)
     if (threadIdx.x < 15) thr[threadIdx.x] = decision_threshold(threadIdx.x);
     __syncthreads();
-    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 16) {
+        const int c = threadIdx.x;
+        const float lo = c == 0 ? -INFINITY : thr[c - 1], hi = c == 15 ? INFINITY : thr[c];
+        bnd[c] = make_float2(c == 0 ? lo : lo + fabsf(lo) * 0x1p-20f, c == 15 ? hi : hi - fabsf(hi) * 0x1p-20f);
+    } else if (threadIdx.x >= 32 && threadIdx.x < 32 + 65) {
+        // bucket j holds the q with round(32 q + 32) = j: q in about [(j - 0.5) / 32 - 1, (j + 0.5) / 32 - 1]
+        const int j = threadIdx.x - 32;
+        const float qlo = (j - 0.5f) / 32.0f - 1.0f, qhi = (j + 0.5f) / 32.0f - 1.0f;
+        const uint32_t c0 = code_of(qlo, thr);
+        const float t = c0 < 15 && thr[c0] <= qhi ? thr[c0] : INFINITY;
+        bkt[j] = make_float2(__uint_as_float(c0), t);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, sub = lane >> 3, l8 = lane & 7;
     const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t g0 = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kQuantGroups;
          g0 < groups; g0 += warps * kQuantGroups) {
-        float2 v[kQuantGroups];
-        float s[kQuantGroups];
+        float4 va[kQuantRounds], vb[kQuantRounds];
 #pragma unroll
-        for (int j = 0; j < kQuantGroups; j++) {
-            v[j] = g0 + j < groups ? __ldcs(reinterpret_cast<const float2*>(w + (g0 + j) * kGroup) + lane)
-                                   : make_float2(0.0f, 0.0f);
+        for (int r = 0; r < kQuantRounds; r++) {
+            const int64_t g = g0 + 4 * r + sub;
+            const float4* src = reinterpret_cast<const float4*>(w + g * kGroup) + 2 * l8;
+            va[r] = g < groups ? __ldcs(src) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            vb[r] = g < groups ? __ldcs(src + 1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
-        for (int j = 0; j < kQuantGroups; j++) s[j] = fmaxf(fabsf(v[j].x), fabsf(v[j].y));
+        for (int r = 0; r < kQuantRounds; r++) {
+            const float x[8] = {va[r].x, va[r].y, va[r].z, va[r].w, vb[r].x, vb[r].y, vb[r].z, vb[r].w};
+            float s = fabsf(x[0]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
+            for (int i = 1; i < 8; i++) s = fmaxf(s, fabsf(x[i]));
 #pragma unroll
-            for (int j = 0; j < kQuantGroups; j++) s[j] = fmaxf(s[j], __shfl_xor_sync(0xFFFFFFFFu, s[j], o));
-        }
-        uint32_t byte[kQuantGroups];
+            for (int o = 1; o < 8; o <<= 1) s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+            const float d = s != 0.0f ? s : 1.0f;
+            float rcp;
+            asm("rcp.approx.f32 %0, %1;" : "=f"(rcp) : "f"(d));
+            // outside [2^-120, 2^120] the reciprocal may leave the normal range: NaN sends every weight
+            // of the group to the exact path
+            if (!(d > 0x1p-120f && d < 0x1p120f)) rcp = __int_as_float(0x7FC00000);
+            uint32_t word = 0;
 #pragma unroll
-        for (int j = 0; j < kQuantGroups; j++) {
-            const float d = s[j] != 0.0f ? s[j] : 1.0f;
-            byte[j] = code_of(__fdiv_rn(v[j].x, d), thr) | (code_of(__fdiv_rn(v[j].y, d), thr) << 4);
-        }
-#pragma unroll
-        for (int j = 0; j < kQuantGroups; j++) {
-            const int64_t g = g0 + j;
+            for (int i = 0; i < 8; i++) word |= fast_code(x[i], rcp, d, thr, bnd, bkt) << (4 * i);
+            const int64_t g = g0 + 4 * r + sub;
             if (g < groups) {
-                codes[g * (kGroup / 2) + lane] = static_cast<uint8_t>(byte[j]);
-                if (lane == 0) scales[g] = __half_as_ushort(__float2half_rn(s[j]));
+                codes[g * (kGroup / 8) + l8] = word;
+                if (l8 == 0) scales[g] = __half_as_ushort(__float2half_rn(s));
             }
         }
     }
@@ -196,8 +236,8 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint8_t* codes
                             int num_sms, cudaStream_t stream) {
     const int64_t groups = N * (K / kGroup);
     if (groups == 0) return cudaSuccess;
-    const int grid = grid_for(8 * kQuantGroups, groups, num_sms, 8);  // 8 warps per 256-thread block
-    quantize_kernel<<<grid, 256, 0, stream>>>(w, groups, codes, scales);
+    const int grid = grid_for(8 * kQuantGroups, groups, num_sms, 5);  // 8 warps per block, 5 blocks resident
+    quantize_kernel<<<grid, 256, 0, stream>>>(w, groups, reinterpret_cast<uint32_t*>(codes), scales);
     return cudaGetLastError();
 }
 

@@ -95,6 +95,29 @@ def test_quantize_every_r_in_unit_interval(nf4):
             assert np.all(f16_dev_to_bits(scales) == 0x3C00)
 
 
+def test_quantize_near_thresholds_any_scale(nf4, o):
+    """Normalised values w / s within a few ulps of every decision threshold, for 4096 random
+    scales s (log-uniform in [1e-3, 1e3], none a power of two): the kernel divides by an approximate
+    reciprocal first and must hand each of these weights to the exact division, so its codes equal
+    the oracle's for all of them."""
+    rng = np.random.default_rng(77)
+    mids = P.decision_thresholds(P.qlora_published_table()).astype(np.float64)  # the 15 fp32 thresholds
+    groups = 4096
+    s = np.exp(rng.uniform(np.log(1e-3), np.log(1e3), groups)).astype(np.float32)
+    s = np.where(np.frexp(s)[0] == 0.5, np.nextafter(s, np.float32(2.0)), s).astype(np.float32)
+    idx = rng.integers(0, 15, (groups, 63))
+    ulp = rng.integers(-40, 41, (groups, 63)).astype(np.float64)
+    r = mids[idx] * (1.0 + ulp * 2.0 ** -23)
+    w = np.empty((groups, 64), np.float32)
+    w[:, 0] = s
+    w[:, 1:] = (r * s[:, None].astype(np.float64)).astype(np.float32)
+    w = w.reshape(512, 8 * 64)
+    codes, scales = gpu_quantize(nf4, w)
+    c_ref, s_ref = o.quantize(w)
+    assert np.array_equal(f16_dev_to_bits(scales), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+
+
 def test_quantize_large_sampled_rows(nf4, o):
     """A 5120 x 27648 matrix (the 32B-shaped down projection) generated on the device: sampled rows
     copied back as fp32 are re-quantized by the oracle."""
