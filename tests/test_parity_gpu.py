@@ -833,10 +833,24 @@ def _host_weights(nf4, seed, n, k):
     return codes, scales, codes.cpu().pin_memory(), scales.cpu().pin_memory()
 
 
+def _bits_to_f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _f64_to_bf16_bits(v):
+    return torch.from_numpy(np.asarray(v, np.float64)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 def test_ring_chain_matches_resident(nf4, o):
     """Five chained M = 1 linears (y of one is x of the next) of different sizes streamed from
-    pinned host memory: every y is bit for bit the resident nf4_linear result, and the first meets
-    the oracle's bound."""
+    pinned host memory: every y is bit for bit the resident nf4_linear result, and every y meets
+    the oracle's bound for a chain the oracle runs itself.
+
+    The oracle's chain feeds its own bf16-rounded y64 forward, never the GPU's y.  Link i + 1 then
+    sees inputs that may differ from the GPU's by delta_k <= tol_i,k + 2^-9 |y64_i,k| (the GPU's
+    error bound plus the oracle's own rounding), which moves the exact sum by at most
+    D = sum_k delta_k |w_hat_k|; the accepted error of link i + 1 is the per-linear bound plus
+    D (1 + 2^-8 + 2^-12), all computed from the oracle's values."""
     from nf4_weight_only_gb300 import synth
     dims = [2048, 2560, 1024, 2048, 11008, 2048]
     mats = [_host_weights(nf4, 300 + i, dims[i + 1], dims[i]) for i in range(len(dims) - 1)]
@@ -860,13 +874,28 @@ def test_ring_chain_matches_resident(nf4, o):
     y64, absum = o.linear(dev_to_bits(x0), c_ref, s_ref, nthreads=16)
     ok, ratio, _ = oracle.within_tolerance(dev_to_bits(ys[0]), y64, absum)
     assert ok, f"oracle bound, linear 0: worst ratio {ratio:.3f}"
+    # the whole chain against the oracle's own chain (see the docstring for the bound)
+    x_o = dev_to_bits(x0)
+    delta = np.zeros(dims[0])
+    for i in range(len(mats)):
+        c_ref, s_ref = o.quantize(synth.device_weights(300 + i, dims[i + 1], dims[i], DEV).cpu().numpy())
+        assert np.array_equal(mats[i][2].numpy(), c_ref), f"packed codes, linear {i}"
+        y64, absum = o.linear(x_o, c_ref, s_ref, nthreads=16)
+        w_abs = np.abs(_bits_to_f64(o.dequant(c_ref, s_ref)))
+        d = w_abs @ delta
+        tol = 2.0 ** -8 * np.abs(y64[0]) + 2.0 ** -12 * absum[0] + d * (1 + 2.0 ** -8 + 2.0 ** -12)
+        err = np.abs(_bits_to_f64(dev_to_bits(ys[i]))[0] - y64[0])
+        assert np.all(err <= tol), f"linear {i}: worst error / bound {np.max(err / tol):.3f}"
+        delta = tol + 2.0 ** -9 * np.abs(y64[0])
+        x_o = _f64_to_bf16_bits(y64)
     assert device_error(nf4) == 0
 
 
 @pytest.mark.parametrize("m", [4, 32])
-def test_ring_small_batch(nf4, m):
-    """M = 4 (GEMV) and M = 32 (tensor-core streaming) through the ring, twelve distinct matrices
-    over two slots, compared with the resident results."""
+def test_ring_small_batch(nf4, o, m):
+    """M = 4 and M = 32 (tensor-core small-M kernel) through the ring, twelve distinct matrices
+    over two slots, compared with the resident results; the first and the last also against the
+    oracle (its own quantization of the same weights, the generator's x)."""
     from nf4_weight_only_gb300 import synth
     n, k = 3072, 2048
     mats = [_host_weights(nf4, 400 + i, n, k) for i in range(12)]
@@ -880,6 +909,12 @@ def test_ring_small_batch(nf4, m):
         nf4.nf4_linear(x, cd, sd, want)
         torch.cuda.synchronize()
         assert torch.equal(want.view(torch.int16), y.view(torch.int16))
+    for i in (0, len(mats) - 1):
+        c_ref, s_ref = o.quantize(synth.device_weights(400 + i, n, k, DEV).cpu().numpy())
+        assert np.array_equal(mats[i][2].numpy(), c_ref)
+        y64, absum = o.linear(dev_to_bits(x), c_ref, s_ref, nthreads=16)
+        ok, ratio, _ = oracle.within_tolerance(dev_to_bits(ys[i]), y64, absum)
+        assert ok, f"matrix {i}: worst ratio {ratio:.3f}"
 
 
 def test_ring_runs_back_to_back_and_in_a_graph(nf4):
