@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             mbar_init(b_dfull + 8 * i, 1);
             mbar_init(b_ep + 8 * i, 4);
         }
-        mbar_init(b_dfree, 4);
+        mbar_init(b_dfree, C::kWide ? 4 * C::kSets : 4);  // every epilogue warp
         mbar_init(b_mdone, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -569,9 +569,11 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
                 }
             }
-            if (!ok || j % C::kSets != set) continue;
+            // wide tiles: every set takes a quarter of the tile's columns in the epilogue (the sets are
+            // idle by then); otherwise set j mod kSets takes all of tile j
+            if (!ok || (!C::kWide && j % C::kSets != set)) continue;
             // ------------------------------------------------------------ epilogue of tile j
-            if (!warp_wait(b_dfull + 8 * set, (j / C::kSets) & 1, wait_ns)) {
+            if (!warp_wait(b_dfull + 8 * (j % C::kSets), (j / C::kSets) & 1, wait_ns)) {
                 record_error(26);
                 ok = false;
                 break;
@@ -581,15 +583,19 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
             uint16_t* y = P.y[p];
             if constexpr (C::kWide) {
-                // The x ring is idle now (one tile per CTA, every MMA done): stage the bf16 tile there
-                // as [token][128 rows], then write whole rows of y with 16-byte stores.
+                // The x ring is idle now (one tile per CTA, every MMA done): each set stages its quarter
+                // of the columns (tokens c0 .. c0 + TC - 1) there as bf16 [token][128 rows], then
+                // writes those tokens' rows of y with 16-byte stores.
                 uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
                 static_assert(C::kXStages * C::kXBytes >= T * 256, "staging tile does not fit the x ring");
-                for (int c = 0; c < T; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem_base + lane_addr + c, v);
+                constexpr int TC = T / C::kSets;
+                static_assert(TC % 16 == 0, "a set's columns are whole 16-column loads");
+                const int c0 = set * TC;
+                for (int c = c0; c < c0 + TC; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem_base + lane_addr + c, v);
 #pragma unroll
-                    for (int cc = 0; cc < 32; cc++) stg[(c + cc) * 128 + i] = bf16_bits(__uint_as_float(v[cc]));
+                    for (int cc = 0; cc < 16; cc++) stg[(c + cc) * 128 + i] = bf16_bits(__uint_as_float(v[cc]));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_ep + 8 * set);
@@ -599,15 +605,16 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     break;
                 }
                 ep_uses++;
+                const int ntok = (M - c0 < TC ? M - c0 : TC) > 0 ? (M - c0 < TC ? M - c0 : TC) : 0;  // this set's tokens
                 if (t.rows == 128 && (np & 7) == 0) {
-                    for (int k = i; k < M * 16; k += 128) {  // token k / 16, 16-byte chunk k % 16
-                        const int tt = k >> 4, cc = k & 15;
+                    for (int k = i; k < ntok * 16; k += 128) {  // token c0 + k / 16, 16-byte chunk k % 16
+                        const int tt = c0 + (k >> 4), cc = k & 15;
                         *reinterpret_cast<uint4*>(y + static_cast<int64_t>(m0 + tt) * np + t.row0 + 8 * cc) =
                             *reinterpret_cast<const uint4*>(stg + tt * 128 + 8 * cc);
                     }
                 } else {
-                    for (int k = i; k < M * t.rows; k += 128) {
-                        const int tt = k / t.rows, rr = k - tt * t.rows;
+                    for (int k = i; k < ntok * t.rows; k += 128) {
+                        const int tt = c0 + k / t.rows, rr = k - (k / t.rows) * t.rows;
                         y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = stg[tt * 128 + rr];
                     }
                 }
