@@ -38,38 +38,34 @@ constexpr uint32_t kLoadBytes = 16384;          // one codes load stage: <= 128 
 constexpr int kMaxProblems = 8;
 constexpr uint64_t kDrainNs = 100000000ull;  // limit of each wait while draining after a timeout (0.1 s)
 
-// Four accumulators: K-step ks of every stage goes to accumulator ks, so that no MMA waits for the
-// previous one to finish (with N of 16..64 an MMA is short); the epilogue adds the four in order.
-constexpr int kAcc = 4;
-
-// T >= 64 ("wide"): a CTA owns one tile of 128 rows x T tokens, N = T per MMA (128 cycles at T = 256,
-// so one accumulator keeps the tensor pipe busy) and no K-slices.
+// Wide tiles (T = 64, 128, 256 tokens): a CTA owns one tile of 128 rows x T tokens, N = T per MMA
+// (128 cycles at T = 256, so one accumulator keeps the tensor pipe busy) and no K-slices.
 template <int T>
 struct Cfg {
-    static constexpr bool kWide = T >= 64;
-    static constexpr int kAccN = kWide ? 1 : kAcc;                    // accumulators
+    static_assert(T >= 64, "the GEMM-form kernel runs wide tiles only (M <= 32 runs nf4_narrow.cuh)");
+    static constexpr bool kWide = true;
+    static constexpr int kAccN = 1;                   // accumulators
     // dequant warp sets (four warps each, one per 32-lane quarter of tensor memory); a set takes
-    // every kSets-th stage, so more sets hide more of the lookups' latency
-    static constexpr int kSets = kWide ? 4 : 3;
+    // every kSets-th stage, so more sets hide more of the dequantization's latency
+    static constexpr int kSets = 4;
     static constexpr int kXWarp = 2 + 4 * kSets;      // the x producer, after the dequant warps
     static constexpr int kThreads = 32 * (kXWarp + 1);
     static constexpr int kTmemCols = 512;
-    static constexpr int kJMax = kWide ? T : (T == 1 ? 16 : (T <= 4 ? 32 : 64));  // columns of B and of each D
-    static constexpr int kSMax = kWide ? 1 : (kJMax / T < 8 ? kJMax / T : 8);      // K-slices per tile
-    static constexpr int kDCols = kAccN * kJMax;                      // accumulators in tensor memory
+    static constexpr int kJMax = T;                   // columns of B and of the accumulator
+    static constexpr int kSMax = 1;                   // K-slices per tile
+    static constexpr int kDCols = kAccN * kJMax;      // accumulator in tensor memory
     // A slots of 64 columns (two groups of K per MMA row); an even count, so that each dequant set
     // owns the same slots in every round
     static constexpr int kAStages = ((kTmemCols - kDCols) / 64 < 8 ? (kTmemCols - kDCols) / 64 : 8) & ~1;
     // ring depths (an x box of T rows takes ~1000-1500 cycles to arrive from L2)
-    static constexpr int kXStages = T <= 4 ? 12 : (T <= 64 ? 8 : (T == 128 ? 6 : 4));  // 64-k x sub-tiles
-    static constexpr int kLoadStages = T <= 128 ? (T == 128 ? 3 : 4) : 3;
+    static constexpr int kXStages = T == 64 ? 8 : (T == 128 ? 6 : 4);  // 64-k x sub-tiles
+    static constexpr int kLoadStages = T == 64 ? 4 : 3;
     static constexpr int kScaleStages = T == 256 ? 2 : 3;
     static constexpr uint32_t kXBytes = kJMax * 128;  // one x sub-tile (multiple of 1024)
     static constexpr uint32_t kOffCodes = kXStages * kXBytes;
     static constexpr uint32_t kOffPtab = kOffCodes + kLoadStages * kLoadBytes;  // half-size pair table
     static constexpr uint32_t kOffScales = kOffPtab + kPairTab16Bytes;
-    static constexpr uint32_t kOffRed = kOffScales + kScaleStages * kScaleSlot;
-    static constexpr uint32_t kOffBars = kOffRed + (kSMax > 1 ? 128 * T * 4 : 0);
+    static constexpr uint32_t kOffBars = kOffScales + kScaleStages * kScaleSlot;
     static constexpr uint32_t kBytes = kOffBars + 1024;
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(8 * (2 * (kLoadStages + kXStages + kAStages + kScaleStages) + 2 * kSets + 2) + 4 <= 1024,
@@ -293,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             mbar_init(b_dfull + 8 * i, 1);
             mbar_init(b_ep + 8 * i, 4);
         }
-        mbar_init(b_dfree, C::kWide ? 4 * C::kSets : 4);  // every epilogue warp
+        mbar_init(b_dfree, 4 * C::kSets);  // every epilogue warp
         mbar_init(b_mdone, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -491,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
         // A set's stages are kSets apart; a load stage holds two stages (S = 1, the only case of the
         // wide tiles) or one, and a scale tile four.
-        static_assert((C::kWide ? (C::kSets + 1) / 2 : C::kSets) <= NL && C::kSets <= 4 && NSS >= 2,
+        static_assert((C::kSets + 1) / 2 <= NL && C::kSets <= 4 && NSS >= 2,
                       "ring too shallow for the release rule");
         static_assert(!C::kWide || C::kSMax == 1, "wide tiles have one K-slice (four sub-stages per load stage)");
         for (int j = 0; j < ntiles && ok; j++) {
@@ -569,9 +565,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
                 }
             }
-            // wide tiles: every set takes a quarter of the tile's columns in the epilogue (the sets are
-            // idle by then); otherwise set j mod kSets takes all of tile j
-            if (!ok || (!C::kWide && j % C::kSets != set)) continue;
+            // every set takes a quarter of the tile's columns in the epilogue (the sets are idle by then)
+            if (!ok) continue;
             // ------------------------------------------------------------ epilogue of tile j
             if (!warp_wait(b_dfull + 8 * (j % C::kSets), (j / C::kSets) & 1, wait_ns)) {
                 record_error(26);
@@ -623,50 +618,6 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 if (lane == 0) mbar_arrive(b_dfree);
                 continue;
             }
-            float* red = reinterpret_cast<float*>(smem + C::kOffRed);
-            const int J = T * t.s;
-            for (int c = 0; c < J; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem_base + lane_addr + c, v);
-#pragma unroll
-                for (int a = 1; a < C::kAccN; a++) {  // add the accumulators in order
-                    uint32_t w[16];
-                    tmem_ld16(tmem_base + lane_addr + a * C::kJMax + c, w);
-#pragma unroll
-                    for (int cc = 0; cc < 16; cc++) v[cc] = __float_as_uint(__uint_as_float(v[cc]) + __uint_as_float(w[cc]));
-                }
-#pragma unroll
-                for (int cc = 0; cc < 16; cc++) {
-                    const int col = c + cc;
-                    if (t.s == 1) {
-                        if (lane_ok && col < M)
-                            y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(__uint_as_float(v[cc]));
-                    } else {
-                        const int rel = col - sl;
-                        const int tt = rel / t.s;
-                        if (rel >= 0 && rel == tt * t.s && tt < M) red[tt * 128 + i] = __uint_as_float(v[cc]);
-                    }
-                }
-            }
-            if (C::kSMax > 1 && t.s > 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_ep + 8 * set);
-                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
-                    record_error(27);
-                    ok = false;
-                    break;
-                }
-                ep_uses++;
-                for (int o = i; o < t.rows * M; o += 128) {
-                    const int tt = o / t.rows, rr = o - tt * t.rows;
-                    float acc = 0.0f;
-                    for (int s2 = 0; s2 < t.s; s2++) acc += red[tt * 128 + rr * t.s + s2];
-                    y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = bf16_bits(acc);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_dfree);
         }
     }
     tc_fence_before();
