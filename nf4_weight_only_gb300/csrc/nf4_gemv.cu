@@ -4,10 +4,11 @@
 // GEMV on CUDA cores and dequantizes only the current tile).  The kernel's job is to consume the
 // packed codes at HBM speed, which leaves about three to four issue slots per weight on a GB300.
 //
-// Dequantization.  The GEMV computes w_hat = bf16(fp32(T[c] * scale)) as the definition states,
-// two weights at a time: a code byte (two codes) indexes a 256-entry shared-memory table whose
-// entry is the fp32 pair {T[low nibble], T[high nibble]}; one packed fp32x2 multiply by the group's
-// scale (round to nearest) and one bf16x2 conversion (round to nearest even) give both weights.
+// Dequantization (helpers in nf4_device.cuh).  The GEMV computes w_hat = bf16(fp32(T[c] * scale))
+// as the definition states, two weights at a time: a code byte (two codes) indexes a 256-entry
+// shared-memory table whose entry is the fp32 pair {T[low nibble], T[high nibble]}; one packed
+// fp32x2 multiply by the group's scale (round to nearest) and one bf16x2 conversion (round to
+// nearest even) give both weights.
 // The table is replicated across the 32 lanes (entry v, lane l at byte 256 v + 8 l), so a warp's
 // 64-bit loads hit 32 distinct bank pairs per half-warp whatever the codes are; one byte permute
 // builds that address from the code word.  Eight weights cost 4 permutes, 4 shared loads, 4 packed

@@ -13,7 +13,7 @@
 //   MMA warp:       tcgen05.mma, A = that w_hat tile in tensor memory, B = x tile in shared memory
 //                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
 //
-// K-slices (as in nf4_stream.cuh).  A CTA owns a contiguous range of output rows, processed as tiles
+// K-slices.  A CTA owns a contiguous range of output rows, processed as tiles
 // of R rows; the 128 MMA rows of a tile are R rows x S K-slices (R * S <= 128): MMA row r * S + s
 // holds row r's groups s, S + s, 2S + s, ...  The B tile holds, for token t and slice s, the x values
 // of group kb*S + s as pseudo-token column t * S + s, and the epilogue adds the S partials of each
