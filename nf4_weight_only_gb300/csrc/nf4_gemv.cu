@@ -580,7 +580,44 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
         }
         return cudaSuccess;
     }
-    if (M > 32) {  // wide tiles: one CTA per 128 rows x T tokens
+    if (M > 32) {  // wide tiles of 128 rows x T tokens
+        // CTAs: one per tile while every token tile's tiles fit the SMs; otherwise each token tile
+        // gets num_sms / (token tiles) CTAs, shared among the problems in proportion to their tiles,
+        // and each CTA walks a balanced run of consecutive tiles (see stream_kernel)
+        const int64_t tsel = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+        const int64_t gy = (M + tsel - 1) / tsel;
+        int64_t tiles[st::kMaxProblems], nc[st::kMaxProblems], total = 0;
+        for (int i = 0; i < count; i++) {
+            tiles[i] = (Ns[i] + 127) / 128;
+            total += tiles[i];
+        }
+        int64_t slots = num_sms / gy;
+        if (slots < count) slots = count;
+        if (total <= slots) {
+            for (int i = 0; i < count; i++) nc[i] = tiles[i];
+        } else {
+            int64_t used = 0;
+            for (int i = 0; i < count; i++) {
+                nc[i] = slots * tiles[i] / total;
+                if (nc[i] < 1) nc[i] = 1;
+                if (nc[i] > tiles[i]) nc[i] = tiles[i];
+                used += nc[i];
+            }
+            while (used < slots) {  // the rest to the problems with the longest runs
+                int best = -1;
+                int64_t best_run = 0;
+                for (int i = 0; i < count; i++) {
+                    const int64_t run = (tiles[i] + nc[i] - 1) / nc[i];
+                    if (nc[i] < tiles[i] && run > best_run) {
+                        best_run = run;
+                        best = i;
+                    }
+                }
+                if (best < 0) break;
+                nc[best]++;
+                used++;
+            }
+        }
         st::Params P = {};
         P.count = count;
         int64_t c = 0;
@@ -590,7 +627,7 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
             P.y[i] = ys[i];
             P.n[i] = static_cast<int>(Ns[i]);
             P.cta0[i] = static_cast<int>(c);
-            c += (Ns[i] + 127) / 128;
+            c += nc[i];
         }
         for (int i = count; i <= st::kMaxProblems; i++) P.cta0[i] = static_cast<int>(c);
         P.rstar = 128;

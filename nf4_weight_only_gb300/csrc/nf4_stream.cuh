@@ -68,7 +68,7 @@ struct Cfg {
     static constexpr uint32_t kOffBars = kOffScales + kScaleStages * kScaleSlot;
     static constexpr uint32_t kBytes = kOffBars + 1024;
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
-    static_assert(8 * (2 * (kLoadStages + kXStages + kAStages + kScaleStages) + 2 * kSets + 2) + 4 <= 1024,
+    static_assert(8 * (2 * (kLoadStages + kXStages + kAStages + kScaleStages) + kSets + 2) + 4 <= 1024,
                   "barrier area");
 };
 
@@ -253,17 +253,23 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
     const uint32_t b_dfull = b_sempty + 8 * NSS;        // [kSets]
     const uint32_t b_dfree = b_dfull + 8 * C::kSets;    // accumulators read (4 warps)
-    const uint32_t b_ep = b_dfree + 8;                  // [kSets] per-set epilogue rendezvous
-    const uint32_t b_mdone = b_ep + 8 * C::kSets;       // every MMA issued has completed
+    const uint32_t b_mdone = b_dfree + 8;               // every MMA issued has completed
     uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + 2 * C::kSets + 2));
+        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + C::kSets + 2));
 
     // this CTA's problem and rows
     int p = 0;
     for (int i = 1; i < P.count; i++)
         if (static_cast<int>(blockIdx.x) >= P.cta0[i]) p = i;
-    const int rbeg = (static_cast<int>(blockIdx.x) - P.cta0[p]) * P.rstar;
-    const int rows_cta = P.n[p] - rbeg < P.rstar ? P.n[p] - rbeg : P.rstar;
+    // a balanced run of the problem's 128-row tiles: one tile when the grid has a CTA per tile,
+    // several consecutive ones otherwise (the CTA then streams a tile's weights and dequantizes its
+    // first stages while the previous tile's last stages and epilogue run)
+    const int nt_p = (P.n[p] + 127) / 128, nc_p = P.cta0[p + 1] - P.cta0[p];
+    const int q_p = static_cast<int>(blockIdx.x) - P.cta0[p];
+    const int t_beg = static_cast<int>(static_cast<int64_t>(q_p) * nt_p / nc_p);
+    const int t_end = static_cast<int>(static_cast<int64_t>(q_p + 1) * nt_p / nc_p);
+    const int rbeg = 128 * t_beg;
+    const int rows_cta = P.n[p] - rbeg < 128 * (t_end - t_beg) ? P.n[p] - rbeg : 128 * (t_end - t_beg);
     const int ntiles = rows_cta / 128 + (rows_cta % 128 != 0);
     const int m0 = static_cast<int>(blockIdx.y) * T;  // first token of this CTA
 
@@ -285,10 +291,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             mbar_init(b_sfull + 8 * i, 32);
             mbar_init(b_sempty + 8 * i, 48);
         }
-        for (int i = 0; i < C::kSets; i++) {
-            mbar_init(b_dfull + 8 * i, 1);
-            mbar_init(b_ep + 8 * i, 4);
-        }
+        for (int i = 0; i < C::kSets; i++) mbar_init(b_dfull + 8 * i, 1);
         mbar_init(b_dfree, 4 * C::kSets);  // every epilogue warp
         mbar_init(b_mdone, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -474,7 +477,6 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         const uint32_t ptab = sbase + C::kOffPtab;                         // shared-window addresses
         const uint32_t lcol16 = static_cast<uint32_t>(lane & 15) * 16;     // twice this lane's copy offset
         bool ok = true;
-        int ep_uses = 0;
         // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
         // ring slots and phases follow from them, so a set visits only its own stages.
         int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
@@ -578,39 +580,21 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
             uint16_t* y = P.y[p];
             if constexpr (C::kWide) {
-                // The x ring is idle now (one tile per CTA, every MMA done): each set stages its quarter
-                // of the columns (tokens c0 .. c0 + TC - 1) there as bf16 [token][128 rows], then
-                // writes those tokens' rows of y with 16-byte stores.
-                uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
-                static_assert(C::kXStages * C::kXBytes >= T * 256, "staging tile does not fit the x ring");
+                // Each set writes a quarter of the tile's token columns (tokens c0 .. c0 + TC - 1)
+                // straight from tensor memory: lane i holds row i, so a warp's store of one token
+                // covers 64 contiguous bytes of y (the x ring may already hold the next tile's x).
                 constexpr int TC = T / C::kSets;
                 static_assert(TC % 16 == 0, "a set's columns are whole 16-column loads");
                 const int c0 = set * TC;
+                const bool row_ok = i < t.rows;
                 for (int c = c0; c < c0 + TC; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tmem_base + lane_addr + c, v);
 #pragma unroll
-                    for (int cc = 0; cc < 16; cc++) stg[(c + cc) * 128 + i] = bf16_bits(__uint_as_float(v[cc]));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_ep + 8 * set);
-                if (!warp_wait(b_ep + 8 * set, ep_uses & 1, wait_ns)) {
-                    record_error(27);
-                    ok = false;
-                    break;
-                }
-                ep_uses++;
-                const int ntok = (M - c0 < TC ? M - c0 : TC) > 0 ? (M - c0 < TC ? M - c0 : TC) : 0;  // this set's tokens
-                if (t.rows == 128 && (np & 7) == 0) {
-                    for (int k = i; k < ntok * 16; k += 128) {  // token c0 + k / 16, 16-byte chunk k % 16
-                        const int tt = c0 + (k >> 4), cc = k & 15;
-                        *reinterpret_cast<uint4*>(y + static_cast<int64_t>(m0 + tt) * np + t.row0 + 8 * cc) =
-                            *reinterpret_cast<const uint4*>(stg + tt * 128 + 8 * cc);
-                    }
-                } else {
-                    for (int k = i; k < ntok * t.rows; k += 128) {
-                        const int tt = c0 + k / t.rows, rr = k - (k / t.rows) * t.rows;
-                        y[static_cast<int64_t>(m0 + tt) * np + t.row0 + rr] = stg[tt * 128 + rr];
+                    for (int cc = 0; cc < 16; cc++) {
+                        const int tt = c + cc;
+                        if (row_ok && tt < M)
+                            y[static_cast<int64_t>(m0 + tt) * np + t.row0 + i] = bf16_bits(__uint_as_float(v[cc]));
                     }
                 }
                 tc_fence_before();
