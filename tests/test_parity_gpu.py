@@ -628,6 +628,37 @@ def test_linear_tensor_core_shapes(nf4, o, n, k):
     assert device_error(nf4) == 0
 
 
+@pytest.mark.parametrize("m,n,k", [(260, 9761, 512), (512, 19583, 256)])
+def test_linear_wide_tile_runs(nf4, o, m, n, k):
+    """More 128-row tiles than a token tile's share of the SMs (77 and 153 tiles against 76 CTAs
+    per token tile): persistent CTAs walk runs of one to three tiles, the last tile ragged."""
+    check_linear(nf4, o, m, n, k, seed=m + n)
+    assert device_error(nf4) == 0
+
+
+def test_linear_grouped_wide_tile_runs(nf4, o):
+    """A grouped call at M = 300 whose problems (5000, 9000 and 130 rows: 40, 71 and 2 tiles) share
+    76 CTAs per token tile in proportion to their tiles; every output meets the oracle bound."""
+    from nf4_weight_only_gb300 import synth
+    k, m = 512, 300
+    ns = [5000, 9000, 130]
+    x = synth.activations_bf16(902, m, k)
+    xd = bf16_to_dev(x)
+    packs, ys = [], []
+    for i, n in enumerate(ns):
+        c, sc = o.quantize(synth.weights(910 + i, n, k))
+        packs.append((c, sc))
+        ys.append(torch.empty((m, n), dtype=torch.bfloat16, device=DEV))
+    nf4.nf4_linear_grouped(xd, [torch.from_numpy(c).to(DEV) for c, _ in packs],
+                           [torch.from_numpy(sc.view(np.int16)).to(DEV).view(torch.float16) for _, sc in packs], ys)
+    torch.cuda.synchronize()
+    for (c, sc), y in zip(packs, ys):
+        y64, mag = o.linear(x, c, sc, nthreads=16)
+        ok, ratio, _ = oracle.within_tolerance(dev_to_bits(y), y64, mag)
+        assert ok, ratio
+    assert device_error(nf4) == 0
+
+
 def test_linear_tensor_core_prefill_sampled(nf4, o):
     """20B-shaped prefill gate projection (6144 -> 16384) at M = 512, checked on sampled outputs."""
     from nf4_weight_only_gb300 import synth
