@@ -583,7 +583,8 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
     if (M > 32) {  // wide tiles of 128 rows x T tokens
         // CTAs: one per tile while every token tile's tiles fit the SMs; otherwise each token tile
         // gets num_sms / (token tiles) CTAs, shared among the problems in proportion to their tiles,
-        // and each CTA walks a balanced run of consecutive tiles (see stream_kernel)
+        // and each CTA walks a balanced run of consecutive tiles (see stream_kernel), unless its
+        // longest run would take more tile times than waves of one-tile CTAs do (many token tiles)
         const int64_t tsel = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
         const int64_t gy = (M + tsel - 1) / tsel;
         int64_t tiles[st::kMaxProblems], nc[st::kMaxProblems], total = 0;
@@ -591,9 +592,8 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
             tiles[i] = (Ns[i] + 127) / 128;
             total += tiles[i];
         }
-        int64_t slots = num_sms / gy;
-        if (slots < count) slots = count;
-        if (total <= slots) {
+        const int64_t slots = num_sms / gy;
+        if (total <= slots || slots < count) {
             for (int i = 0; i < count; i++) nc[i] = tiles[i];
         } else {
             int64_t used = 0;
@@ -617,6 +617,13 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
                 nc[best]++;
                 used++;
             }
+            int64_t longest = 0;
+            for (int i = 0; i < count; i++) {
+                const int64_t run = (tiles[i] + nc[i] - 1) / nc[i];
+                if (run > longest) longest = run;
+            }
+            if (longest > (total * gy + num_sms - 1) / num_sms)
+                for (int i = 0; i < count; i++) nc[i] = tiles[i];
         }
         st::Params P = {};
         P.count = count;
