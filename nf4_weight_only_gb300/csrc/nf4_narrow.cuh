@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    build_pair_table(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -285,11 +286,6 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         // back, so with NA >= kSets the wait for the slot's previous use (NA back) is on a phase whose
         // predecessor has completed.
         static_assert(C::kSets <= NL && C::kSets <= NA, "ring too shallow for the release rule");
-        // The pair table is for the dequant warps alone: they write it while the producers already
-        // stream the first stages, and meet on a named barrier before the first lookup.
-        constexpr int kDqThreads = 32 * 4 * C::kSets;
-        build_pair_table(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x - 128, kDqThreads);
-        asm volatile("bar.sync 1, %0;" ::"r"(kDqThreads) : "memory");
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
             constexpr int lu = 2;                                 // log2 of the sub-stages per load stage

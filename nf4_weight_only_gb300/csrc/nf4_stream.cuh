@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    build_pair_table16(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -488,11 +489,6 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
         // A set's stages are kSets apart; a load stage holds two stages (S = 1, the only case of the
         // wide tiles) or one, and a scale tile four.
-        // The pair table is for the dequant warps alone: they write it while the producers already
-        // stream the first stages, and meet on a named barrier before the first lookup.
-        constexpr int kDqThreads = 32 * 4 * C::kSets;
-        build_pair_table16(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x - 64, kDqThreads);
-        asm volatile("bar.sync 1, %0;" ::"r"(kDqThreads) : "memory");
         static_assert((C::kSets + 1) / 2 <= NL && C::kSets <= 4 && NSS >= 2,
                       "ring too shallow for the release rule");
         static_assert(!C::kWide || C::kSMax == 1, "wide tiles have one K-slice (four sub-stages per load stage)");
