@@ -22,10 +22,11 @@
 //
 // Pipeline stage = 128 k per MMA row (two 64-k sub-stages, 8 MMAs of K = 16).  Stage q uses A slot
 // q mod 4 in tensor memory and x slot q mod 4 in shared memory (both sub-tiles of the stage), so one
-// tcgen05.commit per stage frees both.  Two MMA warps take alternate stages, each into its own pair
-// of accumulators, so that issuing costs the same on two warp schedulers; an issuer waits twice per
-// stage (x landed, A written) and commits once, converged, one elected lane issuing (elect_one).
-// The epilogue adds the four accumulators in a fixed order.
+// tcgen05.commit per stage frees both (on release barrier q mod 12, see the dequant loop).  Two MMA
+// warps take alternate stages, each into its own pair of accumulators, so that issuing costs the
+// same on two warp schedulers; an issuer waits twice per stage (x landed, A written) and commits
+// once, converged, one elected lane issuing (elect_one).  The epilogue adds the four accumulators in
+// a fixed order.
 //
 // Warp roles, one helper per warp scheduler (warp w runs on scheduler w mod 4): warp 0 streams codes
 // (TMA), warps 1 and 3 issue the MMAs of even and odd stages (warp 1 also owns tensor memory), warp 2
@@ -55,6 +56,9 @@ struct NCfg {
     static constexpr int kAStages = 4;                                 // A slots (tensor memory) = x slots
     static constexpr int kLoadStages = 4;                              // codes load stages
     static constexpr int kSets = 3;
+    // release barriers of the A and x slots: stage q's MMAs complete on barrier q mod kRel, a common
+    // multiple of the slots and the sets (see the dequant loop)
+    static constexpr int kRel = kAStages * kSets;
     static constexpr int kThreads = 32 * (4 + 4 * kSets);             // 4 helper warps, one per scheduler
     static constexpr int kU = 4;                                       // 64-k sub-stages per codes load stage
     static constexpr uint32_t kXSub = kJMax * 128;  // one 64-k x sub-tile (multiple of 1024 bytes)
@@ -67,7 +71,7 @@ struct NCfg {
     static_assert(kDCols + 64 * kAStages <= 512, "tensor memory budget");
     static_assert(kAStages == 4 && kLoadStages == 4, "slot arithmetic assumes rings of four");
     static_assert(kSMax == 1 || kSMax == 2 || kSMax == 4 || kSMax == 8, "slices are a power of two");
-    static_assert(8 * (2 * kLoadStages + 3 * kAStages + kSets + 3) + 4 <= 1024, "barrier area");
+    static_assert(8 * (2 * kLoadStages + 2 * kAStages + kRel + kSets + 3) + 4 <= 1024, "barrier area");
 };
 
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane, without waiting for the store.
@@ -101,14 +105,15 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
 
     // barriers
     const uint32_t b_lfull = sbase + C::kOffBars;   // [NL] codes load stage landed (tx)
-    const uint32_t b_lempty = b_lfull + 8 * NL;     // [NL] codes load stage read (weighted releases)
+    const uint32_t b_lempty = b_lfull + 8 * NL;     // [NL] codes load stage passed (every dequant warp)
     const uint32_t b_xfull = b_lempty + 8 * NL;     // [NA] x slot landed (tx)
     const uint32_t b_afull = b_xfull + 8 * NA;      // [NA] A slot written (4 warps)
-    const uint32_t b_empty = b_afull + 8 * NA;      // [NA] A and x slot read by the MMAs (commit)
-    const uint32_t b_dfull = b_empty + 8 * NA;      // [kSets] accumulators complete (both MMA warps), per epilogue set
+    const uint32_t b_rel = b_afull + 8 * NA;        // [kRel] stage q's A and x slots read by its MMAs (commit)
+    const uint32_t b_dfull = b_rel + 8 * C::kRel;   // [kSets] accumulators complete (both MMA warps), per epilogue set
     const uint32_t b_dfree = b_dfull + 8 * C::kSets;  // accumulators read (4 warps)
     const uint32_t b_mdone = b_dfree + 8;           // [2] every MMA an MMA warp issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * NL + 3 * NA + C::kSets + 3));
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * NL + 2 * NA + C::kRel + C::kSets + 3));
 
     // this CTA's problem and rows
     int p = 0;
@@ -123,13 +128,13 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NL; i++) {
             mbar_init(b_lfull + 8 * i, 1);
-            mbar_init(b_lempty + 8 * i, 8);  // weighted releases of the stages that read it
+            mbar_init(b_lempty + 8 * i, 4 * C::kSets);  // every dequant warp, whether it reads the stage or not
         }
         for (int i = 0; i < NA; i++) {
             mbar_init(b_xfull + 8 * i, 1);
             mbar_init(b_afull + 8 * i, 4);
-            mbar_init(b_empty + 8 * i, 1);
         }
+        for (int i = 0; i < C::kRel; i++) mbar_init(b_rel + 8 * i, 1);
         for (int i = 0; i < C::kSets; i++) mbar_init(b_dfull + 8 * i, 2);
         mbar_init(b_dfree, 4);
         mbar_init(b_mdone, 1);
@@ -187,7 +192,9 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         for (int qq = lq - NL > 0 ? lq - NL : 0; qq < lq; qq++) mbar_wait(b_lfull + 8 * (qq & (NL - 1)), (qq >> 2) & 1, kDrainNs);
     } else if (warp == 2) {
         // ---------------------------------------------------------------- x
-        // Stage q's two 64-k sub-tiles land in x slot q mod 4, counted on that slot's own barrier.
+        // Stage q's two 64-k sub-tiles land in x slot q mod 4, counted on that slot's own barrier; the
+        // slot is free once stage q - 4's MMAs have completed (release barrier (q - 4) mod kRel, whose
+        // previous phase this warp saw at stage q - kRel, and whose next needs x of stage q + kRel - 4).
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_full)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&x_rem)) : "memory");
@@ -201,8 +208,8 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const CUtensorMap* xmap = t.s > 1 ? &x_rem : &x_full;
             const uint32_t subbytes = 128u * t.s * T;
             for (int kb2 = 0; kb2 < t.nt / 2; kb2++, q++) {
-                const int slot = q & (NA - 1), round = q >> 2;
-                if (round > 0 && !warp_wait(b_empty + 8 * slot, (round - 1) & 1, wait_ns)) {
+                const int slot = q & (NA - 1);
+                if (q >= NA && !warp_wait(b_rel + 8 * ((q - NA) % C::kRel), ((q - NA) / C::kRel) & 1, wait_ns)) {
                     if (lane == 0) record_error(23);
                     ok = false;
                     break;
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                     const uint64_t b = bdesc + (k8 >= 4 ? (C::kXSub >> 4) : 0) + 2 * (k8 & 3);
                     mma_tmem_a_elect(acc0 + (k8 & 1) * C::kJMax, a_tmem + 8 * k8, b, idesc, !first || k8 >= 2);
                 }
-                mma_commit_elect(b_empty + 8 * slot);
+                mma_commit_elect(b_rel + 8 * (q % C::kRel));
                 first = false;
             }
             if (!ok) break;
@@ -275,17 +282,26 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         // CTA-wide counts of the stages and codes load stages of the tiles before tile j: ring slots
         // and phases follow from them, so a set visits only its own stages.
         int q0 = 0, l0 = 0;
-        // A warp waits only for the codes load stage of its own stages, and its set releases it
-        // after use; the release counts are weighted so that a slot completes when every stage that
-        // reads it is done (8 = two stages of four warps, or one at weight 2).  A parity wait is
-        // sound when the slot's previous fill has completed and its next cannot have: the next needs
-        // this warp's own release, and the previous is complete once the fills are at most NL apart
-        // between consecutive stages of a set, because the warp saw the earlier one.  A set's stages
-        // are kSets apart and a load stage holds two.  The A slot of a stage is reused NA stages
-        // later; a set's previous stage (kSets earlier) waited for the slot of kSets + NA stages
-        // back, so with NA >= kSets the wait for the slot's previous use (NA back) is on a phase whose
-        // predecessor has completed.
-        static_assert(C::kSets <= NL && C::kSets <= NA, "ring too shallow for the release rule");
+        // A parity wait is sound only while the barrier is at most one phase from the awaited one:
+        // the waiter must have seen the phase before it complete, and the phase after it must need
+        // something the waiter has not yet done.
+        //  - Codes load stages: every dequant warp waits for every load stage, whether its set reads
+        //    it or not, and then releases it (b_lempty counts all of them), so the next fill of a
+        //    slot needs its own release, and it saw the slot's previous fill: a set's consecutive
+        //    stages are at most three load stages apart (the two stages between them take at most
+        //    two), so when a warp waits for its own load stage L it has passed every one before the
+        //    previous stage's, L - 4 among them; the load stages between are passed after L (by then
+        //    they have almost always landed, so the warp does not sleep twice).  A set reads at most
+        //    one stage of a load stage (its stages are kSets >= 2 apart).
+        //  - A slots: stage gq waits for the MMAs of stage gq - NA, on release barrier
+        //    (gq - NA) mod kRel.  That barrier's previous phase is stage gq - NA - kRel, which this set
+        //    waited for at its stage gq - kRel (kRel is a multiple of kSets); its next is stage
+        //    gq - NA + kRel, whose A tile waits, through the slot chain, for this stage's MMAs.  The
+        //    MMA warps alternate stages, so a completed stage says nothing about the other warp's
+        //    earlier ones; the wait rule above does not rely on it.
+        static_assert(C::kRel % C::kSets == 0 && C::kRel % NA == 0 && C::kRel >= 2 * NA && C::kSets >= 2,
+                      "release barriers must be a common multiple of the A slots and the sets");
+        int lnext = 0;  // the next codes load stage this warp has not waited for and released
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
             constexpr int lu = 2;                                 // log2 of the sub-stages per load stage
@@ -316,13 +332,17 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 for (int h = 0; h < 2; h++)
                     sc_n2[h] = load_scale(row_scales, ((2 * (kb2 + 2 * C::kSets) + h) << ls) + sl, G, lane_ok);
                 const int gq = q0 + kb2;
-                const int aslot = gq & (NA - 1), around = gq >> 2;
+                const int aslot = gq & (NA - 1);
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
                 const int li = kbs >> lu;                 // its codes load stage, tile-relative
                 const int L = l0 + li;                    // CTA-wide
                 const int lslot = L & (NL - 1);
                 bool good = warp_wait(b_lfull + 8 * lslot, (L >> 2) & 1, wait_ns);
-                if (good && around > 0) good = warp_wait(b_empty + 8 * aslot, (around - 1) & 1, wait_ns);
+                for (; lnext < L && good; lnext++) {       // load stages of the other sets' stages
+                    good = warp_wait(b_lfull + 8 * (lnext & (NL - 1)), (lnext >> 2) & 1, wait_ns);
+                    if (good && lane == 0) mbar_arrive(b_lempty + 8 * (lnext & (NL - 1)));
+                }
+                if (good && gq >= NA) good = warp_wait(b_rel + 8 * ((gq - NA) % C::kRel), ((gq - NA) / C::kRel) & 1, wait_ns);
                 if (!good) {
                     if (lane == 0) record_error(26);
                     ok = false;
@@ -361,10 +381,9 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(b_afull + 8 * aslot);
-                    // a load stage is read by two pipeline stages (weight 1 each), unless it holds
-                    // the tile's last stage alone (weight 2)
-                    mbar_arrive_count(b_lempty + 8 * lslot, nst - 2 * li >= 2 ? 1 : 2);
+                    mbar_arrive(b_lempty + 8 * lslot);
                 }
+                lnext = L + 1;
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     sc_n[h] = sc_n1[h];
@@ -430,6 +449,12 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dfree);
+        }
+        // the load stages after this set's last stage, which the other sets read
+        for (; ok && lnext < l0; lnext++) {
+            ok = warp_wait(b_lfull + 8 * (lnext & (NL - 1)), (lnext >> 2) & 1, wait_ns);
+            if (!ok && lane == 0) record_error(26);
+            if (ok && lane == 0) mbar_arrive(b_lempty + 8 * (lnext & (NL - 1)));
         }
     }
     tc_fence_before();

@@ -13,14 +13,15 @@
 // A CTA owns one tile of 128 rows x T tokens (grid: row tiles x token tiles).  Codes move in load
 // stages of four 64-k sub-stages (one TMA box of 128 rows x 128 bytes), x per 64-k sub-tile (one box
 // of T tokens), scales per 8 sub-stages (zero-filling 16-byte copies of each row's window).  The
-// codes and scale rings are released by the dequant sets whose stages read them, the x ring and the
-// tensor-memory ring of A tiles by the MMAs, so each runs as far ahead as its own consumer allows.
+// codes and scale rings are released by every dequant warp (each passes every fill in order), the
+// x ring and the tensor-memory ring of A tiles by the MMAs, so each runs as far ahead as its own
+// consumers allow.
 //
 // Warp roles: warp 0 streams codes and scales (lane 0 issues the TMA boxes, the warp copies
 // scales), warp 1 owns tensor memory and issues the MMAs (converged, one elected lane), warps
-// 2 .. 4*kSets+1 are kSets = 4 sets of four dequant warps (a set takes every fourth stage and waits
-// only for the codes and scales of its own stages; the four warps of a set cover the four 32-lane
-// quarters of tensor memory), which also run the epilogue, and the last warp streams x.  Weights do
+// 2 .. 4*kSets+1 are kSets = 4 sets of four dequant warps (a set takes every fourth stage; the four
+// warps of a set cover the four 32-lane quarters of tensor memory), which also run the epilogue,
+// and the last warp streams x.  Weights do
 // not depend on the previous kernel in the stream, so warp 0 never waits for it; only x and y do.
 // (The configuration and tile arithmetic below still carry the K-slice fields of the shared tile
 // description, which the wide tiles fix at one slice.)
@@ -57,6 +58,10 @@ struct Cfg {
     // A slots of 64 columns (two groups of K per MMA row); an even count, so that each dequant set
     // owns the same slots in every round
     static constexpr int kAStages = ((kTmemCols - kDCols) / 64 < 8 ? (kTmemCols - kDCols) / 64 : 8) & ~1;
+    // release barriers of the A slots: stage q's MMAs complete on barrier q mod kARel (see the
+    // dequant loop: a multiple of the sets, and two rounds of the slots)
+    static constexpr int kARel = 2 * kAStages;
+    static_assert(kARel % kSets == 0, "the A release barriers must be a multiple of the sets");
     // ring depths (an x box of T rows takes ~1000-1500 cycles to arrive from L2)
     static constexpr int kXStages = T == 64 ? 8 : (T == 128 ? 6 : 4);  // 64-k x sub-tiles
     static constexpr int kLoadStages = T == 64 ? 4 : 3;
@@ -68,7 +73,7 @@ struct Cfg {
     static constexpr uint32_t kOffBars = kOffScales + kScaleStages * kScaleSlot;
     static constexpr uint32_t kBytes = kOffBars + 1024;
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
-    static_assert(8 * (2 * (kLoadStages + kXStages + kAStages + kScaleStages) + kSets + 2) + 4 <= 1024,
+    static_assert(8 * (2 * (kLoadStages + kXStages + kScaleStages) + kAStages + kARel + kSets + 2) + 4 <= 1024,
                   "barrier area");
 };
 
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                   const __grid_constant__ CodeMaps cmaps, const __grid_constant__ Params P) {
     using C = Cfg<T>;
     static_assert(C::kWide, "stream_kernel runs the wide tiles only (T >= 64)");
-    constexpr int NA = C::kAStages, NX = C::kXStages, NL = C::kLoadStages, NSS = C::kScaleStages;
+    constexpr int NA = C::kAStages, NX = C::kXStages, NL = C::kLoadStages, NSS = C::kScaleStages, NR = C::kARel;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -242,20 +247,20 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
 
     // barriers
     const uint32_t b_lfull = sbase + C::kOffBars;       // [NL] codes load stage landed (tx)
-    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage read (its stages' sets)
+    const uint32_t b_lempty = b_lfull + 8 * NL;         // [NL] codes load stage passed (every dequant warp)
     const uint32_t b_xfull = b_lempty + 8 * NL;         // [NX] x tile landed (tx)
     const uint32_t b_xempty = b_xfull + 8 * NX;         // [NX] x tile read by the MMAs (commit)
     const uint32_t b_afull = b_xempty + 8 * NX;         // [NA] A tile in tensor memory (4 warps)
-    const uint32_t b_aempty = b_afull + 8 * NA;         // [NA] A tile read by the MMAs (commit)
-    const uint32_t b_sfull = b_aempty + 8 * NA;         // [NSS] scale tile landed (32 producer lanes)
-    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile read (its stages' sets)
+    const uint32_t b_arel = b_afull + 8 * NA;           // [NR] stage q's A tile read by its MMAs (commit)
+    const uint32_t b_sfull = b_arel + 8 * NR;           // [NSS] scale tile landed (32 producer lanes)
+    const uint32_t b_sempty = b_sfull + 8 * NSS;        // [NSS] scale tile passed (every dequant warp)
     // accumulators complete (commit), one barrier per epilogue set: a set waits only for its own
     // tiles, one phase at a time (a parity wait more than one phase ahead would pass at once)
     const uint32_t b_dfull = b_sempty + 8 * NSS;        // [kSets]
     const uint32_t b_dfree = b_dfull + 8 * C::kSets;    // accumulators read (4 warps)
     const uint32_t b_mdone = b_dfree + 8;               // every MMA issued has completed
     uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NA + NSS) + C::kSets + 2));
+        reinterpret_cast<uint32_t*>(smem + C::kOffBars + 8 * (2 * (NL + NX + NSS) + NA + NR + C::kSets + 2));
 
     // this CTA's problem and rows
     int p = 0;
@@ -277,19 +282,17 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NL; i++) {
             mbar_init(b_lfull + 8 * i, 1);
-            mbar_init(b_lempty + 8 * i, 8);  // weighted releases of the stages that read it
+            mbar_init(b_lempty + 8 * i, 4 * C::kSets);  // every dequant warp, whether it reads the stage or not
         }
         for (int i = 0; i < NX; i++) {
             mbar_init(b_xfull + 8 * i, 1);
             mbar_init(b_xempty + 8 * i, 1);
         }
-        for (int i = 0; i < NA; i++) {
-            mbar_init(b_afull + 8 * i, 4);
-            mbar_init(b_aempty + 8 * i, 1);
-        }
+        for (int i = 0; i < NA; i++) mbar_init(b_afull + 8 * i, 4);
+        for (int i = 0; i < NR; i++) mbar_init(b_arel + 8 * i, 1);
         for (int i = 0; i < NSS; i++) {
             mbar_init(b_sfull + 8 * i, 32);
-            mbar_init(b_sempty + 8 * i, 48);
+            mbar_init(b_sempty + 8 * i, 4 * C::kSets);  // every dequant warp
         }
         for (int i = 0; i < C::kSets; i++) mbar_init(b_dfull + 8 * i, 1);
         mbar_init(b_dfree, 4 * C::kSets);  // every epilogue warp
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         // lane issues each tcgen05.mma and tcgen05.commit (a single diverged lane issuing them took
         // several times longer per instruction on this GPU).
         bool ok = true;
-        int aslot = 0, xslot = 0;
+        int aq = 0, aslot = 0, xslot = 0;  // aq: CTA-wide stage
         uint32_t aph = 0, xph = 0;
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit_elect(b_aempty + 8 * aslot);
+                mma_commit_elect(b_arel + 8 * (aq % NR));
+                aq++;
                 if (++aslot == NA) {
                     aslot = 0;
                     aph ^= 1;
@@ -480,17 +484,20 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         // CTA-wide counts of the stages, codes load stages and scale tiles of the tiles before tile j:
         // ring slots and phases follow from them, so a set visits only its own stages.
         int q0 = 0, l0 = 0, s0 = 0, nst_prev = 0, nload_prev = 0, nscale_prev = 0;
-        // A warp waits only for the codes load stage and the scale tile of its own stages, and its
-        // set releases them after use; the release counts are weighted so that a slot completes when
-        // every stage that reads it is done (a load stage: 8 = two stages of four warps, or one at
-        // weight 2; a scale tile: 48 = n stages of four warps at weight 12 / n).  A parity wait is
-        // sound when the slot's previous fill has completed and its next cannot have: the next
-        // needs this warp's own release, and the previous is complete once the fills are at most
-        // NL (NSS) apart between consecutive stages of a set, because the warp saw the earlier one.
-        // A set's stages are kSets apart; a load stage holds two stages (S = 1, the only case of the
-        // wide tiles) or one, and a scale tile four.
-        static_assert((C::kSets + 1) / 2 <= NL && C::kSets <= 4 && NSS >= 2,
-                      "ring too shallow for the release rule");
+        // A parity wait is sound only while the barrier is at most one phase from the awaited one:
+        // the waiter must have seen the phase before it complete, and the phase after it must need
+        // something the waiter has not yet done.
+        //  - Codes load stages and scale tiles: every dequant warp waits for every fill in order,
+        //    whether its set reads it or not, and then releases it (the empty barriers count all of
+        //    them), so it always saw the slot's previous fill, and the next fill needs its own
+        //    release.  A set reads at most one stage of a load stage (two stages) or a scale tile
+        //    (four), its stages being kSets = 4 apart.  Every set runs every tile's epilogue, and
+        //    passes the tile's remaining fills before it waits for the accumulators.
+        //  - A slots: stage gq waits for the MMAs of stage gq - NA, on release barrier
+        //    (gq - NA) mod NR (NR = 2 NA).  Its previous phase is stage gq - 3 NA, which this set waited
+        //    for at its stage gq - 2 NA (NR is a multiple of kSets); its next is stage gq + NA, whose A
+        //    tile waits for this stage's MMAs.
+        int lnext = 0, snext = 0;  // the next load stage and scale tile this warp has not passed
         static_assert(!C::kWide || C::kSMax == 1, "wide tiles have one K-slice (four sub-stages per load stage)");
         for (int j = 0; j < ntiles && ok; j++) {
             q0 += nst_prev;
@@ -516,15 +523,24 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
             // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets)
             for (int kb2 = (set - q0 % C::kSets + C::kSets) % C::kSets; kb2 < nst && ok; kb2 += C::kSets) {
                 const int gq = q0 + kb2;
-                const int aslot = gq % NA, around = gq / NA;
+                const int aslot = gq % NA;
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
                 const int li = kbs / U;                   // its codes load stage, tile-relative
                 const int si = kbs / 8;                   // its scale tile, tile-relative
                 const int L = l0 + li, S = s0 + si;       // CTA-wide
                 const int lslot = L % NL, sslot = S % NSS;
-                bool good = warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, wait_ns) &&
-                            warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, wait_ns);
-                if (good && around > 0) good = warp_wait(b_aempty + 8 * aslot, (around - 1) & 1, wait_ns);
+                bool good = true;
+                for (; snext < S && good; snext++) {       // fills that only the other sets read
+                    good = warp_wait(b_sfull + 8 * (snext % NSS), (snext / NSS) & 1, wait_ns);
+                    if (good && lane == 0) mbar_arrive(b_sempty + 8 * (snext % NSS));
+                }
+                for (; lnext < L && good; lnext++) {
+                    good = warp_wait(b_lfull + 8 * (lnext % NL), (lnext / NL) & 1, wait_ns);
+                    if (good && lane == 0) mbar_arrive(b_lempty + 8 * (lnext % NL));
+                }
+                good = good && warp_wait(b_sfull + 8 * sslot, (S / NSS) & 1, wait_ns) &&
+                       warp_wait(b_lfull + 8 * lslot, (L / NL) & 1, wait_ns);
+                if (good && gq >= NA) good = warp_wait(b_arel + 8 * ((gq - NA) % NR), ((gq - NA) / NR) & 1, wait_ns);
                 if (!good) {
                     record_error(26);
                     ok = false;
@@ -561,16 +577,26 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(b_afull + 8 * aslot);
-                    const int touching = U == 4 ? (nst - 2 * li < 2 ? nst - 2 * li : 2) : 1;
-                    mbar_arrive_count(b_lempty + 8 * lslot, 2 / touching);
-                    const int stouch = nst - 4 * si < 4 ? nst - 4 * si : 4;
-                    mbar_arrive_count(b_sempty + 8 * sslot, 12 / stouch);
+                    mbar_arrive(b_lempty + 8 * lslot);
+                    mbar_arrive(b_sempty + 8 * sslot);
                 }
+                lnext = L + 1;
+                snext = S + 1;
             }
             // every set takes a quarter of the tile's columns in the epilogue (the sets are idle by then)
             if (!ok) continue;
+            // The tile's remaining fills first: the tile's last stages may need a fill that waits for
+            // this warp's release of an earlier one.
+            for (; ok && snext < s0 + nscale; snext++) {
+                ok = warp_wait(b_sfull + 8 * (snext % NSS), (snext / NSS) & 1, wait_ns);
+                if (ok && lane == 0) mbar_arrive(b_sempty + 8 * (snext % NSS));
+            }
+            for (; ok && lnext < l0 + nload; lnext++) {
+                ok = warp_wait(b_lfull + 8 * (lnext % NL), (lnext / NL) & 1, wait_ns);
+                if (ok && lane == 0) mbar_arrive(b_lempty + 8 * (lnext % NL));
+            }
             // ------------------------------------------------------------ epilogue of tile j
-            if (!warp_wait(b_dfull + 8 * (j % C::kSets), (j / C::kSets) & 1, wait_ns)) {
+            if (!ok || !warp_wait(b_dfull + 8 * (j % C::kSets), (j / C::kSets) & 1, wait_ns)) {
                 record_error(26);
                 ok = false;
                 break;
