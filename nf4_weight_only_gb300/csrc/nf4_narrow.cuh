@@ -147,7 +147,6 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    build_pair_table(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -302,6 +301,11 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         static_assert(C::kRel % C::kSets == 0 && C::kRel % NA == 0 && C::kRel >= 2 * NA && C::kSets >= 2,
                       "release barriers must be a common multiple of the A slots and the sets");
         int lnext = 0;  // the next codes load stage this warp has not waited for and released
+        // The pair table is for the dequant warps alone: they write it while the producers already
+        // stream the first stages, and meet on a named barrier before the first lookup.
+        constexpr int kDqThreads = 32 * 4 * C::kSets;
+        build_pair_table(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x - 128, kDqThreads);
+        asm volatile("bar.sync 1, %0;" ::"r"(kDqThreads) : "memory");
         for (int j = 0; j < ntiles && ok; j++) {
             const Tile t = tile_of(P, rbeg, rows_cta, j);
             constexpr int lu = 2;                                 // log2 of the sub-stages per load stage

@@ -305,7 +305,6 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    build_pair_table16(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x, C::kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -498,6 +497,11 @@ __global__ void __launch_bounds__(Cfg<T>::kThreads, 1)
         //    for at its stage gq - 2 NA (NR is a multiple of kSets); its next is stage gq + NA, whose A
         //    tile waits for this stage's MMAs.
         int lnext = 0, snext = 0;  // the next load stage and scale tile this warp has not passed
+        // The pair table is for the dequant warps alone: they write it while the producers already
+        // stream the first stages, and meet on a named barrier before the first lookup.
+        constexpr int kDqThreads = 32 * 4 * C::kSets;
+        build_pair_table16(reinterpret_cast<float2*>(smem + C::kOffPtab), threadIdx.x - 64, kDqThreads);
+        asm volatile("bar.sync 1, %0;" ::"r"(kDqThreads) : "memory");
         static_assert(!C::kWide || C::kSMax == 1, "wide tiles have one K-slice (four sub-stages per load stage)");
         for (int j = 0; j < ntiles && ok; j++) {
             q0 += nst_prev;
