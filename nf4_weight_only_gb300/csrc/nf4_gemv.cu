@@ -126,11 +126,14 @@ struct GemvLayout {
 // lanes and slices that hold it in a fixed order, writes y and releases the stage.  The consumers
 // thus never wait on a reduction chain, and the result does not depend on the launch shape.
 // Every wait is bounded; after a timeout the waiting thread records an error code and stops.
-// RMAX bounds the rows a consumer warp takes per block (the launcher picks R <= RMAX).
-template <int MT, int LPG, int RMAX>
+// RMAX bounds the rows a consumer warp takes per block (the launcher picks R <= RMAX).  T16 selects
+// the half-size pair table (16 copies, 32 KB; one extra shift per lookup), which leaves room for
+// longer rows in the ring.
+template <int MT, int LPG, int RMAX, bool T16>
 __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ GemvProblems P, int K,
                 const GemvLayout L) {
+    constexpr uint32_t kTab = T16 ? kPairTab16Bytes : kPairTabBytes;  // the table, then the ring
     constexpr int WPL = kGroup / LPG;  // weights per consumer lane per row
     constexpr int CB = WPL / 2;        // code bytes per consumer lane per row
     constexpr int CHUNKS = CB / 16;
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     const int C = L.S * L.Q;
     const int G = K / kGroup;
     const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    uint8_t* ring = smem + kPairTabBytes;
-    const uint32_t bars = sbase + kPairTabBytes + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
+    uint8_t* ring = smem + kTab;
+    const uint32_t bars = sbase + kTab + L.ST * L.stage_bytes;  // full[ST], empty[ST], part[ST]
     // this CTA's rows: a contiguous range, the N rows split as evenly as the grid allows
     const int64_t rbeg = static_cast<int64_t>(N) * blockIdx.x / gridDim.x;
     const int64_t rend = static_cast<int64_t>(N) * (blockIdx.x + 1) / gridDim.x;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                 if (r < rend) {
                     const int pp = problem_of(P, r);
                     const int64_t lr = r - P.row0[pp];
-                    bulk_copy_g2s(sbase + static_cast<uint32_t>(kPairTabBytes + st * L.stage_bytes + j * L.row_code_bytes),
+                    bulk_copy_g2s(sbase + static_cast<uint32_t>(kTab + st * L.stage_bytes + j * L.row_code_bytes),
                                   P.codes[pp] + lr * (K / 2), static_cast<uint32_t>(K / 2), bars + 8 * st);
                     const int64_t sfirst = lr * G * 2;
                     const int64_t a = sfirst & ~static_cast<int64_t>(15);
@@ -256,7 +259,10 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
         const int sw = LPG == 1 ? ((lane >> 2) & 1) : 0;
         // The pair table is for the consumers alone: they write it while the producer already streams
         // the first row blocks, and meet on a named barrier before the first lookup.
-        build_pair_table(reinterpret_cast<float2*>(smem), threadIdx.x, 32 * C);
+        if constexpr (T16)
+            build_pair_table16(reinterpret_cast<float2*>(smem), threadIdx.x, 32 * C);
+        else
+            build_pair_table(reinterpret_cast<float2*>(smem), threadIdx.x, 32 * C);
         pdl_wait();
         uint32_t xr[MT][WPL / 2];
 #pragma unroll
@@ -273,7 +279,8 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(32 * C) : "memory");  // every consumer's table entries written
-        const uint32_t lcol = static_cast<uint32_t>(lane) * 8;  // this lane's column in every table entry
+        // this lane's column in every table entry (twice its copy offset for the half-size table)
+        const uint32_t lcol = T16 ? static_cast<uint32_t>(lane & 15) * 16 : static_cast<uint32_t>(lane) * 8;
         int st = 0, par = 0;  // ring stage of block t and the phase parity of its barriers
         for (int64_t t = 0; t < my_blocks; t++, st = st + 1 == L.ST ? 0 : st + 1, par ^= st == 0) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * st, par, wait_ns))) {
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
                     for (int wi = 0; wi < 4; wi++) {
 #pragma unroll
                         for (int p = 0; p < 4; p++) {
-                            const uint32_t off = pair_offset(words[wi], lcol, p);
+                            const uint32_t off = T16 ? pair_offset16(words[wi], lcol, p) : pair_offset(words[wi], lcol, p);
                             const uint32_t wp = scale_pair(*reinterpret_cast<const float2*>(smem + off), scl[jj]);
 #pragma unroll
                             for (int tt = 0; tt < MT; tt++) fma_bf16x2(a0[tt], a1[tt], wp, xr[tt][4 * (4 * c + wi) + p]);
@@ -340,8 +347,9 @@ __global__ void __launch_bounds__((kMaxWarps + 2) * 32, 1)
     }
 }
 
-template <int MT, int LPG, int RMAX>
+template <int MT, int LPG, int RMAX, bool T16>
 cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, int num_sms, cudaStream_t stream) {
+    constexpr int kTab = T16 ? kPairTab16Bytes : kPairTabBytes;
     constexpr int GPW = 32 / LPG;
     const int64_t N = P.row0[P.count];
     const int G = static_cast<int>(K / kGroup);
@@ -370,7 +378,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
         for (L.R = RMAX;; L.R--) {
             const int64_t q_needed = (N + static_cast<int64_t>(L.R) * num_sms - 1) / (static_cast<int64_t>(L.R) * num_sms);
             L.Q = static_cast<int>(q_needed < 1 ? 1 : (q_needed > qmax ? qmax : q_needed));
-            if (L.R == 1 || (227 * 1024 - kPairTabBytes - 256) / stage_of(L.Q, L.R) >= kMinStages) break;
+            if (L.R == 1 || (227 * 1024 - kTab - 256) / stage_of(L.Q, L.R) >= kMinStages) break;
         }
     } else if (N <= static_cast<int64_t>(2) * kMaxWarps * num_sms) {
         cap_ring = true;
@@ -396,20 +404,20 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     L.stage_bytes = L.red_off + L.S * L.Q * 32 * 4;  // one float per consumer lane
     // ring depth: as many stages as fit next to the pair table in the CTA's share of shared memory (at
     // most 8, at least 2; see cap_ring)
-    const int budget = (half ? kHalfSmem : 227 * 1024) - kPairTabBytes - 3 * 8 * 8 - 64;
+    const int budget = (half ? kHalfSmem : 227 * 1024) - kTab - 3 * 8 * 8 - 64;
     const int64_t blocks_per_cta = ((N + grid64 - 1) / grid64 + L.RB - 1) / L.RB;  // of the largest row range
     L.ST = budget / L.stage_bytes;
     if (L.ST > 8) L.ST = 8;
     if (cap_ring && L.ST > blocks_per_cta) L.ST = static_cast<int>(blocks_per_cta < 2 ? 2 : blocks_per_cta);
     if (L.ST < 2) return cudaErrorInvalidValue;  // a row block does not fit twice
     const int grid = static_cast<int>(grid64);
-    const size_t smem = kPairTabBytes + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
+    const size_t smem = kTab + static_cast<size_t>(L.ST) * L.stage_bytes + 3 * 8 * L.ST;
     static std::once_flag attr_once[64];  // the largest possible request, set once per device
     int dev = 0;
     cudaGetDevice(&dev);
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG, RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<MT, LPG, RMAX, T16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -423,7 +431,7 @@ cudaError_t launch_gemv_t(const uint16_t* x, const GemvProblems& P, int64_t K, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, RMAX>, x, P, static_cast<int>(K), L);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT, LPG, RMAX, T16>, x, P, static_cast<int>(K), L);
 }
 
 }  // namespace
@@ -771,14 +779,21 @@ cudaError_t launch_gemv_grouped(const uint16_t* x, int count, const uint8_t* con
             // K past one slice (32 groups): four rows per warp, else up to two.  Past one slice,
             // two lanes per group (slices of 16 groups) when that leaves fewer lanes idle: K = 5120
             // is 80 groups, three slices of 32 with 16 lanes idle, or five full slices of 16.
-            if (K <= 32 * kGroup) return launch_gemv_t<1, 1, 2>(x, P, K, num_sms, stream);
+            if (K <= 32 * kGroup) return launch_gemv_t<1, 1, 2, false>(x, P, K, num_sms, stream);
             const int64_t G = K / kGroup;
             const int64_t s1 = (G + 31) / 32, s2 = (G + 15) / 16;
-            if (s2 <= kMaxWarps && 16 * s2 < 32 * s1) return launch_gemv_t<1, 2, 4>(x, P, K, num_sms, stream);
-            return launch_gemv_t<1, 1, 4>(x, P, K, num_sms, stream);
+            if (s2 <= kMaxWarps && 16 * s2 < 32 * s1) return launch_gemv_t<1, 2, 4, false>(x, P, K, num_sms, stream);
+            // Rows so long that kMinStages blocks of four rows a warp do not fit beside the 64 KB
+            // table (K past about 20000): the half-size table keeps four rows a warp (27648-wide
+            // rows: 32.6 -> 29.7 us for the 5120-row linear; shorter rows lose by its extra shift).
+            const int64_t swin = ((2 * G + 15) / 16 + 1) * 16;
+            const int64_t stage4 = 4 * (K / 2 + swin + 16) + s1 * 32 * 4;
+            if (kMinStages * stage4 > 227 * 1024 - kPairTabBytes - 256)
+                return launch_gemv_t<1, 1, 4, true>(x, P, K, num_sms, stream);
+            return launch_gemv_t<1, 1, 4, false>(x, P, K, num_sms, stream);
         }
-        case 2: return launch_gemv_t<2, 2, 2>(x, P, K, num_sms, stream);
-        case 3: return launch_gemv_t<3, 2, 2>(x, P, K, num_sms, stream);
+        case 2: return launch_gemv_t<2, 2, 2, false>(x, P, K, num_sms, stream);
+        case 3: return launch_gemv_t<3, 2, 2, false>(x, P, K, num_sms, stream);
         default: return cudaErrorInvalidValue;
     }
 }

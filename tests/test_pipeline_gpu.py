@@ -42,6 +42,7 @@ CASES = [
     # (what, M, rows of each linear, K)
     ("GEMV, M = 1", 1, [5120], 5120),
     ("GEMV, M = 3", 3, [7168], 5120),
+    ("GEMV, M = 1, 27648-wide rows (half-size table)", 1, [5120], 27648),
     ("small-M, one 34-row tile per CTA, two K-slices (14B-shaped q)", 8, [5120], 5120),
     ("small-M grouped 2 x 13824 x 5120", 32, [13824, 13824], 5120),
     ("small-M, K = 16384", 4, [6144], 16384),
