@@ -34,7 +34,7 @@
 // stage; the four warps of a set cover the four 32-lane quarters of tensor memory, one per
 // scheduler) that also run the epilogue of every kSets-th tile.  A set's stage is done when its
 // slowest warp is, so every scheduler carries the same load.  Each dequant thread reads its own
-// group scales from global memory two of its stages ahead (no staging, no barrier).  Weights do not
+// group scales from global memory three of its stages ahead (no staging, no barrier).  Weights do not
 // depend on the previous kernel in the stream, so warp 0 and the scale loads never wait for it;
 // only x and y do.
 // Every mbarrier wait is bounded (wall clock, per wait); a wait that runs out records an error code,
@@ -323,18 +323,19 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
             const uint8_t* crow0 = smem + C::kOffCodes + r * rowb;
             const uint16_t* row_scales = P.scales[p] + static_cast<int64_t>(t.row0 + (lane_ok ? r : 0)) * G;
-            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets); scales two stages ahead
+            // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets); scales three stages ahead
             const int kfirst = (set - q0 % C::kSets + C::kSets) % C::kSets;
-            uint32_t sc_n[2], sc_n1[2], sc_n2[2];
+            uint32_t sc_n[2], sc_n1[2], sc_n2[2], sc_n3[2];
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 sc_n[h] = load_scale(row_scales, ((2 * kfirst + h) << ls) + sl, G, lane_ok);
                 sc_n1[h] = load_scale(row_scales, ((2 * (kfirst + C::kSets) + h) << ls) + sl, G, lane_ok);
+                sc_n2[h] = load_scale(row_scales, ((2 * (kfirst + 2 * C::kSets) + h) << ls) + sl, G, lane_ok);
             }
             for (int kb2 = kfirst; kb2 < nst && ok; kb2 += C::kSets) {
 #pragma unroll
                 for (int h = 0; h < 2; h++)
-                    sc_n2[h] = load_scale(row_scales, ((2 * (kb2 + 2 * C::kSets) + h) << ls) + sl, G, lane_ok);
+                    sc_n3[h] = load_scale(row_scales, ((2 * (kb2 + 3 * C::kSets) + h) << ls) + sl, G, lane_ok);
                 const int gq = q0 + kb2;
                 const int aslot = gq & (NA - 1);
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 for (int h = 0; h < 2; h++) {
                     sc_n[h] = sc_n1[h];
                     sc_n1[h] = sc_n2[h];
+                    sc_n2[h] = sc_n3[h];
                 }
             }
             // which MMA warps had a stage in this tile (the other's accumulators were not written)

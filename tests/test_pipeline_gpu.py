@@ -7,6 +7,8 @@ word).  Each case runs many launches on one stream; every other launch follows a
 larger than L2, so that copy latencies, and with them the warp roles' relative timing, change from
 launch to launch.  The first launch of each case is also checked against the oracle on a few rows.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,7 +18,7 @@ from gpu_util import DEV, dev_to_bits, f16_dev_to_bits
 
 pytestmark = pytest.mark.gpu
 
-LAUNCHES = 120
+LAUNCHES = int(os.environ.get("NF4_STRESS_LAUNCHES", "120"))  # per case; raise it for a longer soak
 
 
 @pytest.fixture(scope="module")
