@@ -535,7 +535,7 @@ cudaError_t launch_stream_t(const uint16_t* x, st::Params& P, int64_t M, int64_t
     void (*kernel)(const CUtensorMap, const CUtensorMap, const st::CodeMaps, const st::Params);
     if constexpr (T <= 32) {
         // the narrow kernel's B tile holds T tokens x s_rem slices (its shared memory is sized for it)
-        if (P.s_rem < 1 || P.s_rem > st::NCfg<T>::kSMax || (P.s_rem & (P.s_rem - 1)) != 0 ||
+        if (P.s_rem < 1 || P.s_rem > st::NCfg<T>::kSMax || 4 * (32 / P.s_rem) < P.r_rem ||
             T * P.s_rem > st::NCfg<T>::kJMax)
             return cudaErrorInvalidValue;
         kBytes = st::NCfg<T>::kBytes;
@@ -684,16 +684,15 @@ cudaError_t launch_stream(const uint16_t* x, int count, const uint8_t* const* co
     P.M = static_cast<int>(M);
     P.K = static_cast<int>(K);
     P.G = static_cast<int>(G);
-    // K-slices of a partial tile: as many as fit 128 MMA rows, the B tile's pseudo-token columns and G.
+    // K-slices of a partial tile: as many as fit the MMA rows (floor(32 / S) rows in each of the four
+    // 32-lane quarters of tensor memory, a row's slices in consecutive lanes), the B tile's
+    // pseudo-token columns (smax) and G.
     P.r_rem = static_cast<int>(rpc % 128);
-    // (a power of two, so that a row's slices are consecutive lanes of one warp)
     auto slices = [&](int smax) {
-        int64_t s = P.r_rem ? 128 / P.r_rem : 1;
-        if (s > smax) s = smax;
-        if (s > G) s = G;
-        int p2 = 1;
-        while (2 * p2 <= s) p2 *= 2;
-        return p2;
+        int best = 1;
+        for (int s = 2; s <= smax && s <= G; s++)
+            if (4 * (32 / s) >= P.r_rem) best = s;
+        return best;
     };
     if (M == 1) {
         P.s_rem = slices(st::NCfg<1>::kSMax);

@@ -14,11 +14,13 @@
 //                   (TMA, 128-byte swizzle), D = fp32 accumulators in tensor memory
 //
 // K-slices.  A CTA owns a contiguous range of output rows, processed as tiles
-// of R rows; the 128 MMA rows of a tile are R rows x S K-slices (R * S <= 128): MMA row r * S + s
-// holds row r's groups s, S + s, 2S + s, ...  The B tile holds, for token t and slice s, the x values
-// of group kb*S + s as pseudo-token column t * S + s, and the epilogue adds the S partials of each
-// (row, token) in slice order.  A CTA with a dozen rows still fills all 128 MMA rows, so the grid is
-// one CTA per SM with a balanced row range each.
+// of R rows; the 128 MMA rows of a tile are R rows x S K-slices: each 32-lane quarter of tensor memory
+// holds floor(32 / S) rows, lane r' * S + s of a quarter holding slice s of its row r', that is row
+// r's groups s, S + s, 2S + s, ...  The B tile holds, for token t and slice s, the x values of group
+// kb*S + s as pseudo-token column t * S + s, and the epilogue adds the S partials of each (row, token)
+// in a fixed order within the warp.  S need not be a power of two: a CTA with 34 rows runs three
+// slices (102 MMA rows) where a power of two would allow two (68).  A CTA with a dozen rows still
+// fills the MMA rows, so the grid is one CTA per SM with a balanced row range each.
 //
 // Pipeline stage = 128 k per MMA row (two 64-k sub-stages, 8 MMAs of K = 16).  Stage q uses A slot
 // q mod 4 in tensor memory and x slot q mod 4 in shared memory (both sub-tiles of the stage), so one
@@ -44,9 +46,9 @@
 namespace nf4 {
 namespace st {
 
-// Ring depths are powers of two (slot and phase arithmetic are masks and shifts).  K-slices are a
-// power of two no larger than kSMax, so a row's slices sit in consecutive lanes of one warp and the
-// epilogue adds them with shuffles.
+// Ring depths are powers of two (slot and phase arithmetic are masks and shifts).  K-slices are at most
+// kSMax, and a row's slices sit in consecutive lanes of one warp, so the epilogue adds them with
+// shuffles.
 template <int T>
 struct NCfg {
     static constexpr int kJMax = T <= 2 ? 16 : (T == 4 ? 32 : 64);  // columns of B and of each D
@@ -70,7 +72,7 @@ struct NCfg {
     static_assert(kBytes + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(kDCols + 64 * kAStages <= 512, "tensor memory budget");
     static_assert(kAStages == 4 && kLoadStages == 4, "slot arithmetic assumes rings of four");
-    static_assert(kSMax == 1 || kSMax == 2 || kSMax == 4 || kSMax == 8, "slices are a power of two");
+    static_assert(kSMax >= 1 && kSMax <= 8, "K-slices");
     static_assert(8 * (2 * kLoadStages + 2 * kAStages + kRel + kSets + 3) + 4 <= 1024, "barrier area");
 };
 
@@ -273,7 +275,6 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
         // ---------------------------------------------------------------- dequant + epilogue
         const int set = (warp - 4) >> 2;
         const int quarter = warp & 3;             // tensor-memory lanes this warp may access
-        const int i = quarter * 32 + lane;        // MMA row
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t ptab = sbase + C::kOffPtab;  // shared-window address of the pair table
         const uint32_t lcol = static_cast<uint32_t>(lane) * 8;  // this lane's column of the pair table
@@ -312,10 +313,12 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const int BS = box_span(t.s);
             const int lbs = BS == 4 ? 2 : (BS == 2 ? 1 : 0);      // log2 BS
             const uint32_t bstride = kLoadBytes >> (lu - lbs);    // a load stage holds 4 / BS boxes
-            const int ls = t.s == 8 ? 3 : (t.s == 4 ? 2 : (t.s == 2 ? 1 : 0));  // log2 S
+            const int S = t.s;
             const int nst = t.nt / 2, nload = (t.nt + C::kU - 1) / C::kU;
-            const int r = i >> ls, sl = i & (t.s - 1);
-            const bool lane_ok = r < t.rows;
+            // row r and slice sl of this lane: floor(32 / S) rows a quarter, S consecutive lanes each
+            const int rq = 32 / S, rl = lane / S, sl = lane - rl * S;
+            const int r = quarter * rq + rl;
+            const bool lane_ok = rl < rq && r < t.rows;
             const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
             // codes of row r in a box: rowb bytes, 16-byte chunks permuted by the 128-byte swizzle
             // (chunk ^ (r mod 8)) when the row is 128 bytes
@@ -328,14 +331,14 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             uint32_t sc_n[2], sc_n1[2], sc_n2[2], sc_n3[2];
 #pragma unroll
             for (int h = 0; h < 2; h++) {
-                sc_n[h] = load_scale(row_scales, ((2 * kfirst + h) << ls) + sl, G, lane_ok);
-                sc_n1[h] = load_scale(row_scales, ((2 * (kfirst + C::kSets) + h) << ls) + sl, G, lane_ok);
-                sc_n2[h] = load_scale(row_scales, ((2 * (kfirst + 2 * C::kSets) + h) << ls) + sl, G, lane_ok);
+                sc_n[h] = load_scale(row_scales, (2 * kfirst + h) * S + sl, G, lane_ok);
+                sc_n1[h] = load_scale(row_scales, (2 * (kfirst + C::kSets) + h) * S + sl, G, lane_ok);
+                sc_n2[h] = load_scale(row_scales, (2 * (kfirst + 2 * C::kSets) + h) * S + sl, G, lane_ok);
             }
             for (int kb2 = kfirst; kb2 < nst && ok; kb2 += C::kSets) {
 #pragma unroll
                 for (int h = 0; h < 2; h++)
-                    sc_n3[h] = load_scale(row_scales, ((2 * (kb2 + 3 * C::kSets) + h) << ls) + sl, G, lane_ok);
+                    sc_n3[h] = load_scale(row_scales, (2 * (kb2 + 3 * C::kSets) + h) * S + sl, G, lane_ok);
                 const int gq = q0 + kb2;
                 const int aslot = gq & (NA - 1);
                 const int kbs = 2 * kb2;                  // first of the stage's two 64-k sub-stages
@@ -361,10 +364,10 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                         const int kb = kbs + h;
                         const int u = kb & (C::kU - 1);  // sub-stage in the load stage: box u / BS
                         uint32_t out[32];
-                        const int g = (kb << ls) + sl;
+                        const int g = kb * S + sl;
                         if (lane_ok && g < G) {
                             const uint8_t* cb = crow + (u >> lbs) * bstride;
-                            const uint32_t ch = static_cast<uint32_t>((((u & (BS - 1)) << ls) + sl) * 2);
+                            const uint32_t ch = static_cast<uint32_t>(((u & (BS - 1)) * S + sl) * 2);
                             const uint4 c0 = lds128(cb + 16 * (ch ^ swz)), c1 = lds128(cb + 16 * ((ch + 1) ^ swz));
                             const float sc = __half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1])));
                             const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -411,7 +414,9 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             pdl_wait();  // y may still be read by the previous grid (returns at once by now)
             const int M = P.M - m0 < T ? P.M - m0 : T, np = P.n[p];  // tokens of this tile
             uint16_t* y = P.y[p];
-            const int J = T * t.s;
+            const int J = T * S;
+            int cm = 0, tt = 0;  // slice and token of column c + cc (K-sliced tiles)
+            float val = 0.0f;    // this lane's slice of the current token
             for (int c = 0; c < J; c += 16) {
                 // accumulators 0 + 1 (even stages), then 2 + 3 (odd stages), then their sum
                 float v[16];
@@ -434,20 +439,28 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                             y[static_cast<int64_t>(m0 + col) * np + t.row0 + r] = bf16_bits(v[cc]);
                     }
                 } else {
-                    // column col = token * S + slice: this lane keeps its own slice's value of each
-                    // token, and after a token's last column the S lanes of the row add theirs with
-                    // shuffles (a fixed order: the result does not depend on timing)
-                    float val = 0.0f;
+                    // column c + cc = token tt * S + slice cm: this lane keeps its own slice's value of
+                    // each token, and after a token's last column the S lanes of the row add theirs
+                    // with shuffles (a fixed order: the result does not depend on timing).  A token's
+                    // columns may straddle two 16-column loads when S does not divide 16.
 #pragma unroll
                     for (int cc = 0; cc < 16; cc++) {
-                        const int col = c + cc;
-                        if ((col & (t.s - 1)) == sl) val = v[cc];
-                        if ((col & (t.s - 1)) == t.s - 1) {  // warp-uniform
-                            float sum = val;
-                            for (int off = 1; off < t.s; off <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-                            const int tt = col >> ls;
+                        if (cm == sl) val = v[cc];
+                        if (cm == S - 1) {  // warp-uniform
+                            float sum;
+                            if ((S & (S - 1)) == 0) {
+                                sum = val;
+                                for (int off = 1; off < S; off <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+                            } else {  // slices 0, 1, ..., S - 1 in order (lanes past the rows read anything)
+                                sum = 0.0f;
+                                for (int jj = 0; jj < S; jj++) sum += __shfl_sync(0xFFFFFFFFu, val, lane - sl + jj);
+                            }
                             if (sl == 0 && lane_ok && tt < M)
                                 y[static_cast<int64_t>(m0 + tt) * np + t.row0 + r] = bf16_bits(sum);
+                            cm = 0;
+                            tt++;
+                        } else {
+                            cm++;
                         }
                     }
                 }

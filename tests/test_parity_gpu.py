@@ -778,6 +778,21 @@ def test_linear_stream_tiles(nf4, o, m, n, k):
     assert device_error(nf4) == 0
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (8, 5168, 1024),   # 34 rows a CTA on 152 SMs: three K-slices (10 rows a tensor-memory quarter)
+    (16, 5168, 1024),  # the same at 16 tokens (48 pseudo-token columns)
+    (4, 3496, 1024),   # 23 rows: five slices
+    (8, 2736, 1024),   # 18 rows: six slices
+    (4, 1824, 448),    # 12 rows, seven groups: seven slices
+    (8, 5120, 13824),  # the 14B-shaped down projection at M = 8
+])
+def test_linear_stream_slices_not_power_of_two(nf4, o, m, n, k):
+    """Partial tiles whose K-slice count is not a power of two: a row's slices sit in consecutive lanes
+    of one tensor-memory quarter, and a token's columns can straddle two 16-column loads."""
+    check_linear(nf4, o, m, n, k, seed=13 * n + k + m)
+    assert device_error(nf4) == 0
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 300, 36864), (1, 19457, 36864), (2, 150, 17408), (3, 2048, 20480),
                                    (4, 129, 17408)])
 def test_linear_stream_long_k(nf4, o, m, n, k):
