@@ -321,10 +321,12 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
             const bool lane_ok = rl < rq && r < t.rows;
             const bool warp_ok = __any_sync(0xFFFFFFFFu, lane_ok);
             // codes of row r in a box: rowb bytes, 16-byte chunks permuted by the 128-byte swizzle
-            // (chunk ^ (r mod 8)) when the row is 128 bytes
+            // (chunk ^ (r mod 8)) when the row is 128 bytes.  A lane past the tile's rows reads row 0
+            // (its A row feeds only its own, unused, row of D).
+            const int rr = lane_ok ? r : 0;
             const uint32_t rowb = 32u * BS * t.s;
-            const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(r & 7) : 0u;
-            const uint8_t* crow0 = smem + C::kOffCodes + r * rowb;
+            const uint32_t swz = rowb == 128 ? static_cast<uint32_t>(rr & 7) : 0u;
+            const uint8_t* crow0 = smem + C::kOffCodes + rr * rowb;
             const uint16_t* row_scales = P.scales[p] + static_cast<int64_t>(t.row0 + (lane_ok ? r : 0)) * G;
             // this set's stages: CTA-wide index q0 + kb2 = set (mod kSets); scales three stages ahead
             const int kfirst = (set - q0 % C::kSets + C::kSets) % C::kSets;
@@ -363,23 +365,19 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                     for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
                         const int kb = kbs + h;
                         const int u = kb & (C::kU - 1);  // sub-stage in the load stage: box u / BS
+                        // Every lane runs the same code: a group past K has scale 0 (its codes and its x
+                        // are zero-filled), so its weights are +-0 and add nothing to the row's sums.
                         uint32_t out[32];
-                        const int g = kb * S + sl;
-                        if (lane_ok && g < G) {
-                            const uint8_t* cb = crow + (u >> lbs) * bstride;
-                            const uint32_t ch = static_cast<uint32_t>(((u & (BS - 1)) * S + sl) * 2);
-                            const uint4 c0 = lds128(cb + 16 * (ch ^ swz)), c1 = lds128(cb + 16 * ((ch + 1) ^ swz));
-                            const float sc = __half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1])));
-                            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        const uint8_t* cb = crow + (u >> lbs) * bstride;
+                        const uint32_t ch = static_cast<uint32_t>(((u & (BS - 1)) * S + sl) * 2);
+                        const uint4 c0 = lds128(cb + 16 * (ch ^ swz)), c1 = lds128(cb + 16 * ((ch + 1) ^ swz));
+                        const float sc = __half2float(__ushort_as_half(static_cast<uint16_t>(h == 0 ? sc_n[0] : sc_n[1])));
+                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                            for (int w = 0; w < 8; w++) {
+                        for (int w = 0; w < 8; w++) {
 #pragma unroll
-                                for (int b = 0; b < 4; b++)
-                                    out[4 * w + b] = scale_pair(lds_f2(ptab + pair_offset(words[w], lcol, b)), sc);
-                            }
-                        } else {
-#pragma unroll
-                            for (int w = 0; w < 32; w++) out[w] = 0u;
+                            for (int b = 0; b < 4; b++)
+                                out[4 * w + b] = scale_pair(lds_f2(ptab + pair_offset(words[w], lcol, b)), sc);
                         }
                         tmem_st32_nowait(tmem_base + lane_addr + C::kDCols + 64 * aslot + 32 * h, out);
                     }
