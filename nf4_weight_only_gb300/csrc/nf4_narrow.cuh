@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(NCfg<T>::kThreads, 1)
                 tc_fence_after();
                 if (warp_ok) {
                     const uint8_t* crow = crow0 + lslot * kLoadBytes;
-#pragma unroll 1
+#pragma unroll
                     for (int h = 0; h < 2; h++) {  // sub-stage kb: A columns 32h .. 32h + 31 of the stage's slot
                         const int kb = kbs + h;
                         const int u = kb & (C::kU - 1);  // sub-stage in the load stage: box u / BS
